@@ -37,7 +37,11 @@ Conventions (readings where the pages are silent, listed in the design doc):
   per-head masks paragraph); it becomes an additive 0 / -inf bias
   ("double-transpose", follow-up item 2, bool mask to additive bias);
 * a query row whose keys are all masked has O = 0, LSE = -inf and contributes
-  no gradient (the pages never reach this case).
+  no gradient (the pages never reach this case);
+* ``attn_fwd`` / ``attn_bwd`` accept a query block of ``Sq`` rows against
+  ``Sk`` keys (rows are independent, so the tests can evaluate sampled query
+  rows of a long sequence exactly; ``dK``/``dV`` are then the contribution of
+  those rows only).
 """
 from __future__ import annotations
 
@@ -128,11 +132,12 @@ def attn_fwd(q, k, v, key_mask=None, scale=None, row_block=_ROW_BLOCK):
     """
     _check_bshd(q, k, v)
     B, S, H, D = q.shape
-    if k.shape != (B, S, H, D) or v.shape != (B, S, H, D):
-        raise ValueError("q, k and v must share one (B, S, H, D) shape")
+    Sk = k.shape[1]
+    if k.shape != (B, Sk, H, D) or v.shape != (B, Sk, H, D):
+        raise ValueError("k and v must be (B, Sk, H, D) with q's B, H, D")
     if scale is None:
         scale = 1.0 / np.sqrt(D)
-    bias = key_bias(key_mask, B, S)
+    bias = key_bias(key_mask, B, Sk)
     o = np.zeros((B, S, H, D), dtype=np.float64)
     lse = np.zeros((B, H, S), dtype=np.float64)
     for b in range(B):
@@ -180,9 +185,12 @@ def attn_bwd(q, k, v, do, key_mask=None, scale=None, row_block=_ROW_BLOCK, retur
     """
     _check_bshd(q, k, v, do)
     B, S, H, D = q.shape
+    Sk = k.shape[1]
+    if k.shape != (B, Sk, H, D) or v.shape != (B, Sk, H, D) or do.shape != q.shape:
+        raise ValueError("k, v must be (B, Sk, H, D) and do must match q")
     if scale is None:
         scale = 1.0 / np.sqrt(D)
-    bias = key_bias(key_mask, B, S)
+    bias = key_bias(key_mask, B, Sk)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)

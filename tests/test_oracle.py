@@ -362,3 +362,17 @@ def test_synth_is_seeded_and_bf16():
     assert ((lens >= 2048) & (lens <= 4096)).all()
     assert m["mask"].shape == (4, 4096)
     assert torch.equal(m["mask"].sum(1).to(torch.int64), lens.to(torch.int64))
+
+
+def test_query_row_subset_is_exact():
+    B, S, H, D = 1, 50, 2, 8
+    q, k, v, do = (rnd((B, S, H, D), s) for s in range(4))
+    mask = (np.arange(S) < 41)[None, :]
+    o, lse = oracle.attn_fwd(q, k, v, mask)
+    dq, _, _ = oracle.attn_bwd(q, k, v, do, mask)
+    rows = np.array([0, 7, 33, 49])
+    o2, lse2 = oracle.attn_fwd(q[:, rows], k, v, mask)
+    dq2, _, _ = oracle.attn_bwd(q[:, rows], k, v, do[:, rows], mask)
+    np.testing.assert_array_equal(o2, o[:, rows])
+    np.testing.assert_array_equal(lse2, lse[:, :, rows])
+    np.testing.assert_allclose(dq2, dq[:, rows], atol=1e-15)
