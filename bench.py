@@ -1,0 +1,390 @@
+"""Throughput of the Ulysses DiT attention hot path on GB300.
+
+One step = one pass of the whole path over the Ulysses emulation workload
+(B=1, N=27280 split into P=4 virtual sequence shards of 6821/6821/6819/6819
+rows, H=40, D=128, bf16 N(0,1) inputs):
+  seq->head exchange of Q, K, V -> attention forward per 10-head group (O, LSE)
+  -> head->seq exchange of O -> seq->head exchange of dO -> attention backward
+  per group (Delta preprocess, K/V-tile-major backward, dQ convert)
+  -> head->seq exchange of dQ, dK, dV.
+Every step runs through the C ABI (``libuaa.so``).
+
+``value`` = attention fwd+bwd FLOPs (4*B*H*S^2*D + 10*B*H*S^2*D) per second of
+the whole step (re-layouts included), inputs resident in HBM.  The inputs
+(4 x 279 MB) are larger than L2 (129 MB), so no L2 flush is added.  ``e2e``
+adds the host->device copy of the step's input shards from pinned memory and
+the device->host copy of O, dQ, dK, dV.  ``--impl reference`` times the fp64
+CPU oracle on bounded samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from ulysses_dit_attention_gb300 import synth  # noqa: E402
+
+WORKLOAD = "ulysses_p4_n27280_h40_d128"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops(B, S, H, D, fwd=True, bwd=True):
+    f = 0
+    if fwd:
+        f += 4 * B * H * S * S * D
+    if bwd:
+        f += 10 * B * H * S * S * D
+    return f
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def _peak_value(d, *keys):
+    for k in keys:
+        v = d.get(k)
+        if isinstance(v, (int, float)) and v > 0:
+            return float(v), k
+    return None, None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (getattr(self, "out", "") or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x):
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_sample(inp, w, seconds=10.0, rows_per_block=512, max_blocks=None):
+    """Times the fp64 oracle on query-row blocks of one head (fwd + bwd), all keys.
+
+    Returns (flops_done, seconds_taken, description).  Rows are independent, so
+    a block of query rows against all keys is a fixed fraction of the workload.
+    """
+    import numpy as np
+
+    import oracle
+
+    h = 0
+    kk = inp["k"][:, :, [h]].float().numpy().astype(np.float64)
+    vv = inp["v"][:, :, [h]].float().numpy().astype(np.float64)
+    done = 0
+    t0 = time.perf_counter()
+    nblk = 0
+    while True:
+        r0 = (nblk * rows_per_block) % w.S
+        r1 = min(w.S, r0 + rows_per_block)
+        qq = inp["q"][:, r0:r1, [h]].float().numpy().astype(np.float64)
+        dd = inp["do"][:, r0:r1, [h]].float().numpy().astype(np.float64)
+        oracle.attn_fwd(qq, kk, vv, None, w.scale)
+        oracle.attn_bwd(qq, kk, vv, dd, None, w.scale)
+        done += 14 * (r1 - r0) * w.S * w.D
+        nblk += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_blocks and nblk >= max_blocks):
+            break
+    desc = (f"fp64 NumPy oracle, fwd+bwd of {nblk} block(s) of {rows_per_block} query rows x {w.S} keys of "
+            f"head {h} (D={w.D}); FLOPs counted as 14*rows*S*D")
+    return done, el, desc
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = synth.workload(WORKLOAD)
+    inp = synth.make(w)
+    times, fl = [], []
+    for i in range(args.warmup + args.steps):
+        f, t, desc = oracle_sample(inp, w, seconds=0.0, rows_per_block=256, max_blocks=1)
+        if i >= args.warmup:
+            times.append(t)
+            fl.append(f)
+    value = sum(fl) / sum(times) / 1e12
+    line = {"metric": "attention fwd+bwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "B": w.B, "N": w.S, "P": w.P, "H": w.H, "D": w.D,
+                       "shard_lens": list(w.shard_lens)},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, world, rank, local):
+    import ulysses_dit_attention_gb300 as uaa
+    from ulysses_dit_attention_gb300 import build as uaa_build
+
+    uaa_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.workload(WORKLOAD)
+    B, S, H, D, P = w.B, w.S, w.H, w.D, w.P
+    lens, cap, Hg = w.shard_lens, w.cap, w.H // w.P
+    inp = synth.make(w)
+    host = {n: synth.pad_shards(inp[n], lens, cap).pin_memory() for n in ("q", "k", "v", "do")}
+    sh = {n: t.to(dev) for n, t in host.items()}
+    # device buffers of the step (allocated once; the step itself allocates nothing)
+    yq, yk, yv, ydo = (torch.empty((P, B, S, Hg, D), dtype=torch.bfloat16, device=dev) for _ in range(4))
+    yo, ydq, ydk, ydv = (torch.empty_like(yq) for _ in range(4))
+    lse = torch.empty((P, B, Hg, S), dtype=torch.float32, device=dev)
+    o_sh, dq_sh, dk_sh, dv_sh = (torch.empty_like(sh["q"]) for _ in range(4))
+    ws = torch.empty(uaa.attn_bwd_workspace_bytes(B, S, Hg, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = {}
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(name, []).append(e)
+
+    def step(timed=False):
+        if timed:
+            mark("s2h_fwd0")
+        for n, y in (("q", yq), ("k", yk), ("v", yv)):
+            uaa.seq_to_head(sh[n], lens, out=y)
+        if timed:
+            mark("s2h_fwd1")
+        for g in range(P):
+            if timed:
+                mark("fwd0")
+            uaa.attn_fwd(yq[g], yk[g], yv[g], None, w.scale, out=yo[g], lse=lse[g])
+            if timed:
+                mark("fwd1")
+        if timed:
+            mark("h2s_o0")
+        uaa.head_to_seq(yo, lens, cap, out=o_sh)
+        uaa.seq_to_head(sh["do"], lens, out=ydo)
+        if timed:
+            mark("h2s_o1")
+        for g in range(P):
+            if timed:
+                mark("bwd0")
+            uaa.attn_bwd(yq[g], yk[g], yv[g], yo[g], ydo[g], lse[g], None, w.scale, dq=ydq[g], dk=ydk[g],
+                         dv=ydv[g], workspace=ws)
+            if timed:
+                mark("bwd1")
+        if timed:
+            mark("h2s_g0")
+        for y, x in ((ydq, dq_sh), (ydk, dk_sh), (ydv, dv_sh)):
+            uaa.head_to_seq(y, lens, cap, out=x)
+        if timed:
+            mark("h2s_g1")
+
+    launches_per_step = 3 + P + 1 + 1 + 3 * P + 3
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    uaa.check_device_status(dev)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(timed=True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    uaa.check_device_status(dev)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(world, ms)
+
+    def pair_ms(a, b):
+        return sum(x.elapsed_time(y) for x, y in zip(ev[a], ev[b]))
+
+    fwd_ms = pair_ms("fwd0", "fwd1") / args.steps
+    bwd_ms = pair_ms("bwd0", "bwd1") / args.steps
+    fwd_launch = pair_ms("fwd0", "fwd1") / len(ev["fwd0"])
+    bwd_launch = pair_ms("bwd0", "bwd1") / len(ev["bwd0"])
+    relayout_ms = (pair_ms("s2h_fwd0", "s2h_fwd1") + pair_ms("h2s_o0", "h2s_o1") +
+                   pair_ms("h2s_g0", "h2s_g1")) / args.steps
+    tensor_bytes = B * S * H * D * 2
+    relayout_bytes = 8 * 2 * tensor_bytes + 4 * (P * B * cap * H * D * 2 - tensor_bytes)  # + padding zero fill
+    step_flops = flops(B, S, H, D)
+    value = world * step_flops / (ms * 1e-3) / 1e12
+
+    # e2e through the same public calls with host buffers: H2D of the input shards, D2H of O/dQ/dK/dV
+    outs_host = {n: torch.empty_like(host["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+
+    def e2e_step():
+        for n in ("q", "k", "v", "do"):
+            sh[n].copy_(host[n], non_blocking=True)
+        step()
+        for n, t in (("o", o_sh), ("dq", dq_sh), ("dk", dk_sh), ("dv", dv_sh)):
+            outs_host[n].copy_(t, non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    uaa.check_device_status(dev)
+
+    pk, src = peaks()
+    peak_tf, key = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops")
+    peak_hbm, _ = _peak_value(pk, "hbm_gbs")
+    bwd_flops_launch = flops(B, S, Hg, D, fwd=False)
+    achieved = bwd_flops_launch / (bwd_launch * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": None,
+                "kernel": "uaa_attn_bwd (Delta preprocess + K/V-tile-major backward + dQ convert), one head group",
+                "peak_source": f"{src} {key}"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        f, t, desc = oracle_sample(inp, w, seconds=args.cpu_seconds)
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+    line = {
+        "metric": "attention fwd+bwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "N": S, "P": P, "H": H, "D": D, "shard_lens": list(lens),
+                   "cap": cap, "mask": None, "l2": "inputs larger than L2 (4 x 279 MB shards), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU, 4 emulated Ulysses ranks"},
+        "parts_ms_per_step": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms, "relayout": relayout_ms},
+        "attn_fwd_tflops": flops(B, S, H, D, bwd=False) / (fwd_ms * 1e-3) / 1e12,
+        "attn_bwd_tflops": flops(B, S, H, D, fwd=False) / (bwd_ms * 1e-3) / 1e12,
+        "fwd_launch_tflops": flops(B, S, Hg, D, bwd=False) / (fwd_launch * 1e-3) / 1e12,
+        "relayout_gbs": relayout_bytes / (relayout_ms * 1e-3) / 1e9,
+        "relayout_hbm_frac": (relayout_bytes / (relayout_ms * 1e-3) / 1e9) / peak_hbm if peak_hbm else None,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="uaa", choices=["uaa", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "uaa" else args.warmup
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+/*
+ * uaa.h -- C ABI of the GB300 (sm_103a) Ulysses DiT attention library.
+ *
+ * The library implements the data-parallel hot path discussed in three
+ * pull-request pages:
+ *   - "[attention] Add Ulysses Anything backward" (diffusers PR 14834),
+ *     cited below as "UAA-bwd";
+ *   - "Add fast-ulysses attention backend" (LightX2V PR 1234), "fast-ulysses";
+ *   - "Fix double transpose of K/V in templated attention backward"
+ *     (diffusers PR 14341), "double-transpose".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Attention tensors are BSHD: (B, S, H, D) contiguous, bf16, row stride
+ *    H*D elements.  The forward op returns its output in BSHD and the backward
+ *    consumes Q, K, V in that same layout ("double-transpose", description).
+ *  - D must be 64 or 128.  Non-causal, no dropout ("double-transpose",
+ *    Not verified: non-causal, no dropout).
+ *  - lse is fp32 (B, H, S): the natural log of sum_j exp(scale*q.k_j + bias_j).
+ *  - key_mask is an optional uint8 (B, S) array, nonzero = attend.  It is the
+ *    head-broadcast (B, 1, 1, S) key-padding mask ("UAA-bwd", Unsupported cases,
+ *    per-head masks) and acts as an additive 0 / -inf bias
+ *    ("double-transpose", follow-up item 2).  A query row whose keys are all
+ *    masked gets O = 0, LSE = -inf and no gradient.
+ *  - All pointers marked "device" are device memory owned by the caller; the
+ *    library never allocates or frees device memory.  Host arrays
+ *    (shard_lens) are read during the call only.
+ *  - Work is enqueued on `stream` and is asynchronous; nothing synchronises
+ *    the stream except uaa_check_device_status().
+ *  - Every entry point validates its arguments on the host first.  A negative
+ *    status from validation means nothing was launched.  The message for the
+ *    last non-OK status of the calling thread is in uaa_last_error().
+ *  - Device-side waits (mbarrier / TMA / tensor-core completion) are bounded.
+ *    A wait that runs out records UAA_ERR_TIMEOUT in a device status word and
+ *    the kernel returns; uaa_check_device_status() reports and clears it.
+ *
+ * Pointer alignment: every device pointer must be 16-byte aligned (the TMA
+ * loads and the 16-byte vector copies need it).
+ */
+#ifndef UAA_H_
+#define UAA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA stream handle (cudaStream_t / CUstream); 0 = the legacy default stream. */
+typedef void* uaa_stream_t;
+
+typedef enum {
+  UAA_OK = 0,
+  UAA_ERR_INVALID_ARG = -1,   /* bad pointer, size, shape or alignment */
+  UAA_ERR_UNSUPPORTED = -2,   /* valid request outside what is built (D not 64/128, H % P != 0) */
+  UAA_ERR_PER_HEAD_MASK = -3, /* a (B, H>1, 1, S) mask: Ulysses cannot shard it ("UAA-bwd",
+                                 What does this PR do: fail fast on per-head masks) */
+  UAA_ERR_CUDA = -4,          /* a CUDA runtime / driver call failed */
+  UAA_ERR_TIMEOUT = -5        /* a bounded device-side wait ran out (reported by
+                                 uaa_check_device_status) */
+} uaa_status;
+
+/* Attention forward.
+ * "double-transpose", description: the forward op returns out in BSHD and the
+ * backward needs the log-sum-exp; its follow-up item 1 shows what goes wrong
+ * when the LSE is not computed, so this call ALWAYS writes lse (no flag).
+ *   q, k, v  : device, bf16 (B, S, H, D)
+ *   key_mask : device, uint8 (B, S) or NULL (no mask)
+ *   out      : device, bf16 (B, S, H, D)
+ *   lse      : device, fp32 (B, H, S)
+ *   scale    : softmax scale applied to q.k (the usual value is 1/sqrt(D))
+ * Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                 void* out, float* lse, int B, int S, int H, int D, float scale,
+                 uaa_stream_t stream);
+
+/* Bytes of device workspace uaa_attn_bwd needs for (B, S, H, D):
+ * an fp32 (B, H, S) row-dot vector Delta = rowsum(dO * O) followed (at a
+ * 256-byte aligned offset) by an fp32 (B, S, H, D) dQ accumulator.
+ * Returns 0 for invalid sizes. */
+size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D);
+
+/* Attention backward: dQ, dK, dV from dO, O and LSE.
+ * "double-transpose", description: the backward op receives Q, K, V in one
+ * layout (no second transpose of K/V), dO in BSHD and the saved LSE.
+ *   q, k, v, out, dout : device, bf16 (B, S, H, D)
+ *   lse                : device, fp32 (B, H, S), as written by uaa_attn_fwd
+ *   key_mask           : device, uint8 (B, S) or NULL; must be the mask the
+ *                        forward used.  Masked keys get dK = dV = 0 exactly.
+ *   dq, dk, dv         : device, bf16 (B, S, H, D), written (not accumulated)
+ *   workspace          : device, at least uaa_attn_bwd_workspace_bytes() bytes,
+ *                        256-byte aligned; contents on entry are ignored
+ * Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                 const void* dout, const float* lse, const uint8_t* key_mask,
+                 void* dq, void* dk, void* dv, int B, int S, int H, int D, float scale,
+                 void* workspace, size_t workspace_bytes, uaa_stream_t stream);
+
+/* Ulysses forward exchange on one device: sequence shards -> head groups.
+ * "UAA-bwd", What does this PR do (all-to-all with saved partition metadata,
+ * uneven shards); "fast-ulysses", Summary (A2A around the attention module).
+ *   x : device (P, B, cap, H, D) -- shard p's rows s < shard_lens[p] are valid,
+ *       rows s >= shard_lens[p] are transport padding (not read)
+ *   y : device (P, B, N, H/P, D), N = sum(shard_lens); group g holds heads
+ *       [g*H/P, (g+1)*H/P) of every valid row, shards concatenated in rank order:
+ *       y[g, b, off_p + s, h', :] = x[p, b, s, g*H/P + h', :]
+ *   shard_lens : host, P ints, 0 <= shard_lens[p] <= cap
+ *   elem_bytes : bytes per element (2 for bf16, 4 for fp32); D*elem_bytes must
+ *       be a multiple of 16
+ * H % P != 0 (padded heads) returns UAA_ERR_UNSUPPORTED.  x and y must not
+ * overlap.  Bit-exact copy. */
+int uaa_seq_to_head(const void* x, void* y, int P, const int* shard_lens, int cap,
+                    int B, int H, int D, int elem_bytes, uaa_stream_t stream);
+
+/* Ulysses inverse exchange: head groups -> sequence shards (exact inverse of
+ * uaa_seq_to_head).  Padding rows s >= shard_lens[p] of every shard are
+ * written as zero.  Used for O in the forward and for dQ (query partition) and
+ * dK/dV (key partition) in the backward ("UAA-bwd", What does this PR do). */
+int uaa_head_to_seq(const void* y, void* x, int P, const int* shard_lens, int cap,
+                    int B, int H, int D, int elem_bytes, uaa_stream_t stream);
+
+/* Key-padding mask assembly from gathered per-rank shards, trimming every
+ * shard to its true length BEFORE concatenation ("UAA-bwd", What does this PR
+ * do: the uneven mask-assembly fix; Validation: the four-rank masked case).
+ *   gathered : device uint8 (P, B, cap)
+ *   mask     : device uint8 (B, N), N = sum(shard_lens)
+ *   mask[b, off_p + s] = gathered[p, b, s] for s < shard_lens[p]. */
+int uaa_assemble_key_mask(const uint8_t* gathered, uint8_t* mask, int P, const int* shard_lens,
+                          int cap, int B, uaa_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * words.  Returns UAA_OK, UAA_ERR_TIMEOUT (a bounded device wait ran out in
+ * some kernel since the last check) or UAA_ERR_CUDA. */
+int uaa_check_device_status(uaa_stream_t stream);
+
+/* Diagnostic for the watchdog: launches one block whose thread waits on an
+ * mbarrier that nothing arrives on, with a wait bound of `timeout_us`
+ * microseconds (1..1000000).  The wait runs out, the kernel records
+ * UAA_ERR_TIMEOUT and returns; no copy or tensor-core work is in flight. */
+int uaa_watchdog_selftest(unsigned int timeout_us, uaa_stream_t stream);
+
+/* Sets the bound (in milliseconds, default 4000) of every device-side wait in
+ * the kernels launched afterwards by the calling process. 0 restores the default. */
+void uaa_set_wait_timeout_ms(unsigned int ms);
+
+/* Thread-local, NUL-terminated message for the last non-OK status returned to
+ * the calling thread ("" if none).  Owned by the library. */
+const char* uaa_last_error(void);
+
+/* Library version string, e.g. "uaa 0.1 sm_103a". */
+const char* uaa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UAA_H_ */

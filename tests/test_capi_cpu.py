@@ -1,0 +1,105 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every symbol that
+``include/uaa.h`` declares, and rejects bad arguments on the host before any
+CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ulysses_dit_attention_gb300 as uaa
+from ulysses_dit_attention_gb300 import build as uaa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    uaa_build.build()
+    return uaa.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "uaa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(uaa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.uaa_version().decode().startswith("uaa")
+
+
+def test_workspace_bytes(L):
+    B, S, H, D = 1, 27280, 40, 128
+    got = L.uaa_attn_bwd_workspace_bytes(B, S, H, D)
+    delta = (B * H * S * 4 + 255) // 256 * 256
+    assert got == delta + B * S * H * D * 4
+    assert L.uaa_attn_bwd_workspace_bytes(1, 16, 2, 96) == 0
+
+
+def _err():
+    return uaa.lib().uaa_last_error().decode()
+
+
+def test_attn_fwd_rejects_bad_args_on_host(L):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    st = L.uaa_attn_fwd(fake, fake, fake, None, fake, fake, 1, 16, 2, 96, ctypes.c_float(0.1), None)
+    assert st == -2 and "D=96" in _err()
+    st = L.uaa_attn_fwd(fake, fake, fake, None, fake, fake, 1, 16, 2, 64, ctypes.c_float(-1.0), None)
+    assert st == -1 and "scale" in _err()
+    st = L.uaa_attn_fwd(None, fake, fake, None, fake, fake, 1, 16, 2, 64, ctypes.c_float(0.125), None)
+    assert st == -1 and "q is NULL" in _err()
+    st = L.uaa_attn_fwd(P((1 << 20) + 8), fake, fake, None, fake, fake, 1, 16, 2, 64, ctypes.c_float(0.125), None)
+    assert st == -1 and "aligned" in _err()
+    # empty input: nothing to do, nothing launched
+    assert L.uaa_attn_fwd(None, None, None, None, None, None, 0, 16, 2, 64, ctypes.c_float(0.125), None) == 0
+    assert L.uaa_attn_fwd(None, None, None, None, None, None, 2, 0, 2, 64, ctypes.c_float(0.125), None) == 0
+
+
+def test_attn_bwd_rejects_small_workspace(L):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    ws = P(1 << 24)
+    st = L.uaa_attn_bwd(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, 1, 256, 2, 64,
+                        ctypes.c_float(0.125), ws, 16, None)
+    assert st == -1 and "workspace" in _err()
+    st = L.uaa_attn_bwd(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, 1, 256, 2, 64,
+                        ctypes.c_float(0.125), P((1 << 24) + 16), 1 << 30, None)
+    assert st == -1 and "256-byte" in _err()
+
+
+def test_relayout_rejects_bad_partitions_on_host(L):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    lens = (ctypes.c_int * 4)(6821, 6821, 6819, 6819)
+    # H % P != 0: padded heads are not built
+    assert L.uaa_seq_to_head(fake, fake, 4, lens, 6821, 1, 42, 128, 2, None) == -2
+    # a shard longer than the capacity
+    assert L.uaa_seq_to_head(fake, fake, 4, lens, 6820, 1, 40, 128, 2, None) == -1
+    assert "cap" in _err()
+    # D * elem_bytes not a multiple of 16
+    assert L.uaa_head_to_seq(fake, fake, 4, lens, 6821, 1, 40, 4, 2, None) == -1
+    # negative shard length
+    bad = (ctypes.c_int * 2)(3, -1)
+    assert L.uaa_assemble_key_mask(fake, fake, 2, bad, 3, 1, None) == -1
+    assert L.uaa_watchdog_selftest(0, None) == -1
+
+
+def test_python_binding_rejects_per_head_mask_before_launch():
+    import torch
+    with pytest.raises(ValueError, match="per-head"):
+        uaa.normalize_key_mask(torch.ones(2, 4, 1, 16, dtype=torch.bool), 2, 16)
+    m = uaa.normalize_key_mask(torch.ones(2, 1, 1, 16, dtype=torch.bool), 2, 16)
+    assert m.dtype == torch.uint8 and tuple(m.shape) == (2, 16)
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        uaa.attn_fwd(q, q, q)

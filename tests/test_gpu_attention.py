@@ -1,0 +1,212 @@
+"""GPU attention forward/backward (through the C ABI) vs the fp64 oracle.
+
+Small and ragged cases are compared element by element on every output; the
+large workloads (S = 4096 masked, S = 27280) are compared exactly on sampled
+heads (heads are independent, so the oracle evaluates just those heads) and on
+sampled query rows; the Ulysses emulation is checked against the oracle and,
+bit for bit, against the plain full-sequence path.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ulysses_dit_attention_gb300 as uaa
+from ulysses_dit_attention_gb300 import synth
+from helpers import bits, compare, f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def run_gpu(inp, scale, mask):
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    m = None if mask is None else mask.to(DEV)
+    o, lse = uaa.attn_fwd(q, k, v, m, scale)
+    dq, dk, dv = uaa.attn_bwd(q, k, v, o, do, lse, m, scale)
+    uaa.check_device_status()
+    return o, lse, dq, dk, dv
+
+
+def check_against_oracle(inp, mask, scale, heads=None, label=""):
+    o, lse, dq, dk, dv = run_gpu(inp, scale, mask)
+    sel = slice(None) if heads is None else list(heads)
+    q, k, v, do = (f64(inp[n])[:, :, sel] for n in ("q", "k", "v", "do"))
+    m = None if mask is None else mask.numpy().astype(bool)
+    ro, rl = oracle.attn_fwd(q, k, v, m, scale)
+    rdq, rdk, rdv = oracle.attn_bwd(q, k, v, do, m, scale)
+    res = {}
+    res["o"] = compare(f"{label} O", f64(o)[:, :, sel], ro, "o")
+    res["lse"] = compare(f"{label} LSE", f64(lse)[:, sel], rl, "lse")
+    res["dq"] = compare(f"{label} dQ", f64(dq)[:, :, sel], rdq, "dq")
+    res["dk"] = compare(f"{label} dK", f64(dk)[:, :, sel], rdk, "dk")
+    res["dv"] = compare(f"{label} dV", f64(dv)[:, :, sel], rdv, "dv")
+    if m is not None:
+        # masked keys receive exactly zero dK / dV
+        dkn, dvn = f64(dk), f64(dv)
+        for b in range(m.shape[0]):
+            assert (dkn[b, ~m[b]] == 0).all() and (dvn[b, ~m[b]] == 0).all()
+    return res
+
+
+SMALL = [
+    # B, S, H, D, mask kind
+    (2, 16, 16, 64, None),        # layout trap: H == S
+    (1, 1, 1, 64, None),          # single token
+    (1, 127, 2, 128, None),       # one ragged tile
+    (2, 129, 3, 64, "prefix"),    # two tiles, ragged, prefix mask
+    (1, 300, 2, 128, "random"),   # three tiles, arbitrary (non-prefix) mask
+    (2, 257, 2, 128, "empty_b1"), # batch 1 fully masked: O = 0, LSE = -inf, no grads
+    (1, 640, 4, 64, "prefix"),    # mask ends inside a tile, whole masked tiles
+]
+
+
+@pytest.mark.parametrize("B,S,H,D,kind", SMALL)
+def test_small_and_ragged_cases(B, S, H, D, kind):
+    inp = synth.draw(B, S, H, D, seed=1000 + S + H, masked=False)
+    mask = None
+    g = torch.Generator().manual_seed(S)
+    if kind == "prefix":
+        lens = torch.randint(S // 2, S + 1, (B,), generator=g)
+        lens[0] = max(1, S // 3)
+        mask = (torch.arange(S)[None, :] < lens[:, None]).to(torch.uint8)
+    elif kind == "random":
+        mask = (torch.rand((B, S), generator=g) < 0.5).to(torch.uint8)
+    elif kind == "empty_b1":
+        mask = torch.ones((B, S), dtype=torch.uint8)
+        mask[1] = 0
+        mask[0, 200:] = 0
+    check_against_oracle(inp, mask, 1.0 / math.sqrt(D), label=f"B{B} S{S} H{H} D{D} {kind}")
+    if kind == "empty_b1":
+        o, lse, dq, dk, dv = run_gpu(inp, 1.0 / math.sqrt(D), mask)
+        assert (f64(o)[1] == 0).all() and np.isneginf(f64(lse)[1]).all()
+        assert (f64(dq)[1] == 0).all() and (f64(dk)[1] == 0).all() and (f64(dv)[1] == 0).all()
+
+
+def test_non_default_scale():
+    inp = synth.draw(1, 200, 2, 64, seed=7)
+    check_against_oracle(inp, None, 0.37, label="scale 0.37")
+
+
+def test_layout_workload_full():
+    w = synth.workload("layout_b2_s16_h16_d64")
+    check_against_oracle(synth.make(w), None, w.scale, label=w.name)
+
+
+def test_dit_1k_workload_full():
+    w = synth.workload("dit_b2_s1024_h24_d64")
+    check_against_oracle(synth.make(w), None, w.scale, label=w.name)
+
+
+def test_mask_workload_sampled_heads():
+    w = synth.workload("mask_b4_s4096_h24_d128")
+    inp = synth.make(w)
+    check_against_oracle(inp, inp["mask"], w.scale, heads=[0, 11, 23], label=w.name)
+
+
+def test_forward_is_deterministic_and_writes_lse():
+    inp = synth.draw(1, 513, 2, 128, seed=3)
+    a = run_gpu(inp, 1 / math.sqrt(128), None)
+    b = run_gpu(inp, 1 / math.sqrt(128), None)
+    for x, y in zip(a, b):
+        if x is a[2]:
+            continue  # dQ is accumulated with atomics (order may vary)
+        assert np.array_equal(bits(x), bits(y))
+    assert np.isfinite(f64(a[1])).all()
+
+
+@pytest.mark.parametrize("name", ["dit_b1_s27280_h40_d128"])
+def test_dit_27k_workload_sampled(name):
+    w = synth.workload(name)
+    inp = synth.make(w)
+    o, lse, dq, dk, dv = run_gpu(inp, w.scale, None)
+    # one whole head, every output, exactly
+    h = [w.H - 1]
+    q, k, v, do = (f64(inp[n])[:, :, h] for n in ("q", "k", "v", "do"))
+    ro, rl = oracle.attn_fwd(q, k, v, None, w.scale)
+    rdq, rdk, rdv = oracle.attn_bwd(q, k, v, do, None, w.scale)
+    compare("O", f64(o)[:, :, h], ro, "o")
+    compare("LSE", f64(lse)[:, h], rl, "lse")
+    compare("dQ", f64(dq)[:, :, h], rdq, "dq")
+    compare("dK", f64(dk)[:, :, h], rdk, "dk")
+    compare("dV", f64(dv)[:, :, h], rdv, "dv")
+    # sampled query rows of two more heads: O, LSE and dQ rows are exact per row
+    rows = np.array([0, 1, 127, 128, 13653, 27151, 27152, 27279])
+    for hh in (0, 17):
+        qs = f64(inp["q"])[:, rows][:, :, [hh]]
+        dos = f64(inp["do"])[:, rows][:, :, [hh]]
+        kk, vv = f64(inp["k"])[:, :, [hh]], f64(inp["v"])[:, :, [hh]]
+        ro, rl = oracle.attn_fwd(qs, kk, vv, None, w.scale)
+        rdq, _, _ = oracle.attn_bwd(qs, kk, vv, dos, None, w.scale)
+        compare(f"O rows h{hh}", f64(o)[:, rows][:, :, [hh]], ro, "o")
+        compare(f"LSE rows h{hh}", f64(lse)[:, [hh]][:, :, rows], rl, "lse")
+        compare(f"dQ rows h{hh}", f64(dq)[:, rows][:, :, [hh]], rdq, "dq")
+
+
+def test_ulysses_emulation_workload():
+    """seq->head, attention per 10-head group, head->seq; fwd + bwd.
+
+    The forward equals the full-sequence path bit for bit (same inputs, the
+    head groups are exact head slices); dK/dV too (deterministic); dQ is
+    accumulated with atomics, so it is compared with the tolerance.
+    """
+    w = synth.workload("ulysses_p4_n27280_h40_d128")
+    inp = synth.make(w)
+    lens, cap = w.shard_lens, w.cap
+    sh = {n: synth.pad_shards(inp[n], lens, cap).to(DEV) for n in ("q", "k", "v", "do")}
+    q_sh = sh["q"].requires_grad_(True)
+    k_sh = sh["k"].requires_grad_(True)
+    v_sh = sh["v"].requires_grad_(True)
+    o_sh, lse_g = uaa.ulysses_attention(q_sh, k_sh, v_sh, lens, None, w.scale)
+    o_sh.backward(sh["do"])
+    uaa.check_device_status()
+    # padding rows of every returned shard are zero
+    for p, L in enumerate(lens):
+        for t in (o_sh, q_sh.grad, k_sh.grad, v_sh.grad):
+            assert (bits(t[p, :, L:]) == 0).all()
+    # reference: the plain path on the unsharded sequence
+    o, lse, dq, dk, dv = run_gpu(inp, w.scale, None)
+
+    def unshard(t):
+        return torch.cat([t[p, :, :L] for p, L in enumerate(lens)], dim=1)
+
+    assert np.array_equal(bits(unshard(o_sh.detach())), bits(o))
+    hg = w.H // w.P
+    for g in range(w.P):
+        assert np.array_equal(bits(lse_g[g]), bits(lse[:, g * hg:(g + 1) * hg]))
+    assert np.array_equal(bits(unshard(k_sh.grad)), bits(dk))
+    assert np.array_equal(bits(unshard(v_sh.grad)), bits(dv))
+    d = (unshard(q_sh.grad).float() - dq.float()).abs().max().item()
+    assert d <= 4e-3, d
+    # and the oracle on one head of the last group, through the oracle's own exchange
+    h = [w.H - 3]
+    q, k, v, do = (f64(inp[n])[:, :, h] for n in ("q", "k", "v", "do"))
+    rdq, rdk, rdv = oracle.attn_bwd(q, k, v, do, None, w.scale)
+    ro, _ = oracle.attn_fwd(q, k, v, None, w.scale)
+    compare("ulysses O", f64(unshard(o_sh.detach()))[:, :, h], ro, "o")
+    compare("ulysses dQ", f64(unshard(q_sh.grad))[:, :, h], rdq, "dq")
+    compare("ulysses dK", f64(unshard(k_sh.grad))[:, :, h], rdk, "dk")
+    compare("ulysses dV", f64(unshard(v_sh.grad))[:, :, h], rdv, "dv")
+
+
+def test_autograd_function_marks_lse_non_differentiable():
+    inp = synth.draw(1, 64, 2, 64, seed=9)
+    q, k, v = (inp[n].to(DEV).requires_grad_(True) for n in ("q", "k", "v"))
+    out, lse = uaa.attention(q, k, v)
+    assert not lse.requires_grad
+    out.backward(inp["do"].to(DEV))
+    dq, dk, dv = uaa.attn_bwd(q.detach(), k.detach(), v.detach(), out.detach(), inp["do"].to(DEV), lse)
+    assert np.array_equal(bits(k.grad), bits(dk)) and np.array_equal(bits(v.grad), bits(dv))
+
+
+def test_watchdog_reports_timeout_and_context_survives():
+    assert uaa.watchdog_selftest(2000) == 0
+    with pytest.raises(uaa.UAAError) as e:
+        uaa.check_device_status()
+    assert e.value.status == -5
+    uaa.check_device_status()  # cleared
+    inp = synth.draw(1, 64, 1, 64, seed=1)
+    run_gpu(inp, 0.125, None)  # the context is still usable

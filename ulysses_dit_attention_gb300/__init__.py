@@ -1,1 +1,321 @@
-"""GB300-native Ulysses DiT attention (placeholder; the binding lands with the C-ABI)."""
+"""GB300-native Ulysses DiT attention: thin Python binding over the ``libuaa.so`` C ABI.
+
+Every step of the computation runs in the library's sm_103a kernels; this module
+only marshals arguments (shapes, dtypes, pointers, the current CUDA stream) and
+allocates outputs/workspace with PyTorch.  There is no CPU or eager fallback: if
+the library is not built, or the tensors are not on a CUDA device, calls raise.
+
+Names follow the C ABI (``include/uaa.h``): ``attn_fwd``, ``attn_bwd``,
+``seq_to_head``, ``head_to_seq``, ``assemble_key_mask``; ``Attention`` is the
+``torch.autograd.Function`` pairing them (the LSE output is marked
+non-differentiable, as in "[attention] Add Ulysses Anything backward", What does
+this PR do), and ``ulysses_attention`` composes the Ulysses exchange around it
+for P emulated ranks on one device.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "seq_to_head", "head_to_seq",
+    "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms", "Attention",
+    "attention", "UlyssesAttention", "ulysses_attention", "STATUS",
+]
+
+STATUS = {0: "UAA_OK", -1: "UAA_ERR_INVALID_ARG", -2: "UAA_ERR_UNSUPPORTED", -3: "UAA_ERR_PER_HEAD_MASK",
+          -4: "UAA_ERR_CUDA", -5: "UAA_ERR_TIMEOUT"}
+
+
+class UAAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "uaa_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "uaa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "uaa_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P,
+                          ctypes.c_size_t, _P]),
+    "uaa_seq_to_head": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "uaa_head_to_seq": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "uaa_assemble_key_mask": (_I, [_P, _P, _I, _P, _I, _I, _P]),
+    "uaa_check_device_status": (_I, [_P]),
+    "uaa_watchdog_selftest": (_I, [ctypes.c_uint, _P]),
+    "uaa_set_wait_timeout_ms": (None, [ctypes.c_uint]),
+    "uaa_last_error": (ctypes.c_char_p, []),
+    "uaa_version": (ctypes.c_char_p, []),
+}
+
+
+def lib():
+    """Load ``libuaa.so`` (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lib_lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                       "`python -m ulysses_dit_attention_gb300.build` (no fallback exists)")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGS.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise UAAError(status, lib().uaa_last_error().decode(errors="replace"))
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("uaa kernels run on CUDA tensors only (no CPU fallback)")
+
+
+def _bshd(name, t, ref=None):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be (B, S, H, D), got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous BSHD")
+    if ref is not None and t.shape != ref.shape:
+        raise ValueError(f"{name} shape {tuple(t.shape)} differs from {tuple(ref.shape)}")
+
+
+def normalize_key_mask(mask, B, S):
+    """Key mask -> contiguous uint8 ``(B, S)``.
+
+    Accepts ``(B, S)`` or the head-broadcast ``(B, 1, 1, S)`` form; a per-head
+    ``(B, H>1, 1, S)`` mask raises ``ValueError`` before any launch ("[attention]
+    Add Ulysses Anything backward", What does this PR do: fail fast on per-head
+    masks, which Ulysses cannot shard).  A bool mask is reinterpreted as bytes
+    (no copy kernel).
+    """
+    if mask is None:
+        return None
+    if mask.dim() == 4:
+        if mask.shape[1] != 1 or mask.shape[2] != 1:
+            raise ValueError(f"per-head attention masks {tuple(mask.shape)} are not supported: only "
+                             "head-broadcast (B, 1, 1, S) key masks can be sharded across heads")
+        mask = mask.reshape(mask.shape[0], mask.shape[3])
+    if mask.dim() != 2 or tuple(mask.shape) != (B, S):
+        raise ValueError(f"key mask must be (B, S) = {(B, S)}, got {tuple(mask.shape)}")
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    if mask.dtype != torch.uint8:
+        raise TypeError("key mask must be bool or uint8")
+    if not mask.is_contiguous():
+        raise ValueError("key mask must be contiguous")
+    return mask
+
+
+# --------------------------------------------------------------------------- attention
+def attn_fwd(q, k, v, key_mask=None, scale=None, out=None, lse=None):
+    """``uaa_attn_fwd``: returns ``(out bf16 (B,S,H,D), lse fp32 (B,H,S))``."""
+    _bshd("q", q)
+    _bshd("k", k, q)
+    _bshd("v", v, q)
+    _need_cuda(q, k, v)
+    B, S, H, D = q.shape
+    mask = normalize_key_mask(key_mask, B, S)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    _check(lib().uaa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), B, S, H, D,
+                              float(scale), _P(_stream(q.device))))
+    return out, lse
+
+
+def attn_bwd_workspace_bytes(B, S, H, D) -> int:
+    return int(lib().uaa_attn_bwd_workspace_bytes(B, S, H, D))
+
+
+def attn_bwd(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """``uaa_attn_bwd``: returns ``(dq, dk, dv)`` in bf16 BSHD."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _bshd(n, t, q)
+    _need_cuda(q, k, v, out, dout, lse)
+    B, S, H, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 (B, H, S)")
+    mask = normalize_key_mask(key_mask, B, S)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    nbytes = attn_bwd_workspace_bytes(B, S, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(lib().uaa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, S, H, D, float(scale), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _P(_stream(q.device))))
+    return dq, dk, dv
+
+
+class Attention(torch.autograd.Function):
+    """Autograd pairing of ``attn_fwd`` / ``attn_bwd``; ``lse`` is non-differentiable."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, key_mask=None, scale=None):
+        out, lse = attn_fwd(q, k, v, key_mask, scale)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.key_mask = key_mask
+        ctx.scale = scale
+        ctx.mark_non_differentiable(lse)
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, _dlse):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, out, dout.contiguous(), lse, ctx.key_mask, ctx.scale)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, key_mask=None, scale=None):
+    return Attention.apply(q, k, v, key_mask, scale)
+
+
+# --------------------------------------------------------------------------- Ulysses re-layout
+def _lens_array(shard_lens):
+    lens = [int(x) for x in shard_lens]
+    return (ctypes.c_int * len(lens))(*lens), lens
+
+
+def seq_to_head(x, shard_lens, out=None):
+    """``uaa_seq_to_head``: ``(P, B, cap, H, D)`` shards -> ``(P, B, N, H/P, D)`` groups."""
+    _need_cuda(x)
+    if x.dim() != 5 or not x.is_contiguous():
+        raise ValueError("x must be contiguous (P, B, cap, H, D)")
+    P, B, cap, H, D = x.shape
+    arr, lens = _lens_array(shard_lens)
+    if len(lens) != P:
+        raise ValueError("len(shard_lens) must equal P")
+    if H % P:
+        raise ValueError(f"H={H} must be divisible by P={P} (padded heads are not implemented)")
+    N = sum(lens)
+    if out is None:
+        out = torch.empty((P, B, N, H // P, D), dtype=x.dtype, device=x.device)
+    _check(lib().uaa_seq_to_head(_ptr(x), _ptr(out), P, arr, cap, B, H, D, x.element_size(), _P(_stream(x.device))))
+    return out
+
+
+def head_to_seq(y, shard_lens, cap, out=None):
+    """``uaa_head_to_seq``: ``(P, B, N, H/P, D)`` groups -> ``(P, B, cap, H, D)`` shards (padding zeroed)."""
+    _need_cuda(y)
+    if y.dim() != 5 or not y.is_contiguous():
+        raise ValueError("y must be contiguous (P, B, N, H/P, D)")
+    P, B, N, Hg, D = y.shape
+    arr, lens = _lens_array(shard_lens)
+    if len(lens) != P or sum(lens) != N:
+        raise ValueError("shard_lens must have P entries summing to N")
+    if out is None:
+        out = torch.empty((P, B, cap, Hg * P, D), dtype=y.dtype, device=y.device)
+    _check(lib().uaa_head_to_seq(_ptr(y), _ptr(out), P, arr, cap, B, Hg * P, D, y.element_size(),
+                                 _P(_stream(y.device))))
+    return out
+
+
+def assemble_key_mask(gathered, shard_lens, out=None):
+    """``uaa_assemble_key_mask``: gathered ``(P, B, cap)`` uint8 -> trimmed ``(B, N)`` uint8."""
+    _need_cuda(gathered)
+    if gathered.dtype == torch.bool:
+        gathered = gathered.view(torch.uint8)
+    if gathered.dim() != 3 or gathered.dtype != torch.uint8 or not gathered.is_contiguous():
+        raise ValueError("gathered must be contiguous uint8 (P, B, cap)")
+    P, B, cap = gathered.shape
+    arr, lens = _lens_array(shard_lens)
+    if len(lens) != P:
+        raise ValueError("len(shard_lens) must equal P")
+    if out is None:
+        out = torch.empty((B, sum(lens)), dtype=torch.uint8, device=gathered.device)
+    _check(lib().uaa_assemble_key_mask(_ptr(gathered), _ptr(out), P, arr, cap, B, _P(_stream(gathered.device))))
+    return out
+
+
+def check_device_status(device=None):
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    _check(lib().uaa_check_device_status(_P(_stream(dev))))
+
+
+def watchdog_selftest(timeout_us=2000, device=None):
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return lib().uaa_watchdog_selftest(int(timeout_us), _P(_stream(dev)))
+
+
+def set_wait_timeout_ms(ms: int):
+    lib().uaa_set_wait_timeout_ms(int(ms))
+
+
+# --------------------------------------------------------------------------- Ulysses composition
+class UlyssesAttention(torch.autograd.Function):
+    """Ulysses attention over P emulated ranks on one device.
+
+    Forward: seq->head exchange of Q, K, V; attention per head group (all groups
+    share the assembled key mask); head->seq exchange of O.  Backward: seq->head
+    exchange of dO; attention backward per group; head->seq exchange of dQ
+    (query partition) and dK, dV (key partition).  "[attention] Add Ulysses
+    Anything backward", What does this PR do.
+    """
+
+    @staticmethod
+    def forward(ctx, q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):
+        cap = q_sh.shape[2]
+        yq, yk, yv = (seq_to_head(t, shard_lens) for t in (q_sh, k_sh, v_sh))
+        P = yq.shape[0]
+        o = torch.empty_like(yq)
+        lse = torch.empty((P, yq.shape[1], yq.shape[3], yq.shape[2]), dtype=torch.float32, device=yq.device)
+        for g in range(P):
+            attn_fwd(yq[g], yk[g], yv[g], key_mask, scale, out=o[g], lse=lse[g])
+        o_sh = head_to_seq(o, shard_lens, cap)
+        ctx.save_for_backward(yq, yk, yv, o, lse)
+        ctx.shard_lens, ctx.key_mask, ctx.scale, ctx.cap = tuple(shard_lens), key_mask, scale, cap
+        ctx.mark_non_differentiable(lse)
+        return o_sh, lse
+
+    @staticmethod
+    def backward(ctx, do_sh, _dlse):
+        yq, yk, yv, o, lse = ctx.saved_tensors
+        ydo = seq_to_head(do_sh.contiguous(), ctx.shard_lens)
+        P = yq.shape[0]
+        dq, dk, dv = torch.empty_like(yq), torch.empty_like(yq), torch.empty_like(yq)
+        g0 = yq[0]
+        ws = torch.empty(attn_bwd_workspace_bytes(*g0.shape), dtype=torch.uint8, device=yq.device)
+        for g in range(P):
+            attn_bwd(yq[g], yk[g], yv[g], o[g], ydo[g], lse[g], ctx.key_mask, ctx.scale, dq=dq[g], dk=dk[g],
+                     dv=dv[g], workspace=ws)
+        return (head_to_seq(dq, ctx.shard_lens, ctx.cap), head_to_seq(dk, ctx.shard_lens, ctx.cap),
+                head_to_seq(dv, ctx.shard_lens, ctx.cap), None, None, None)
+
+
+def ulysses_attention(q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):
+    return UlyssesAttention.apply(q_sh, k_sh, v_sh, tuple(shard_lens), key_mask, scale)

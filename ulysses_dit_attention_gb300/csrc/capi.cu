@@ -1,0 +1,148 @@
+// Host side of the C ABI that is shared by every kernel family: the per-thread
+// last-error message, the per-device status word (the target of the kernels'
+// bounded-wait watchdog), the wait bound, TMA tensor-map encoding for BSHD
+// tensors, and the watchdog self-test kernel.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "uaa_common.cuh"
+
+namespace uaa {
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+// The status word: one per device, a file-scope device variable of this
+// translation unit.  Its device address is looked up once per device.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+unsigned int* g_status_addr[kMaxDevices] = {nullptr};
+
+std::atomic<unsigned long long> g_timeout_ns{4000ull * 1000ull * 1000ull};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+int set_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return UAA_OK;
+}
+
+int get_dev_ctx(DevCtx* ctx) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return set_error(UAA_ERR_CUDA, "device index %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_status_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_status_word);
+      if (e != cudaSuccess)
+        return set_error(UAA_ERR_CUDA, "cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
+      g_status_addr[dev] = static_cast<unsigned int*>(p);
+    }
+    ctx->status = g_status_addr[dev];
+  }
+  ctx->timeout_ns = g_timeout_ns.load();
+  return UAA_OK;
+}
+
+int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  // dims innermost first: D (contiguous), H, S, B; a box is 64 elements of D
+  // (one 128-byte swizzle row) x 1 head x box_rows positions x 1 batch.
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return UAA_OK;
+}
+
+// One thread waits on an mbarrier that nothing arrives on; the bounded wait
+// runs out and records a timeout.  No copy or tensor-core work is issued.
+__global__ void watchdog_selftest_kernel(DevCtx ctx) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, ctx.timeout_ns)) atomicOr(ctx.status, kStatusTimeout);
+  }
+}
+
+}  // namespace uaa
+
+using namespace uaa;
+
+extern "C" {
+
+const char* uaa_last_error(void) { return g_last_error; }
+
+const char* uaa_version(void) { return "uaa 0.1 sm_103a"; }
+
+void uaa_set_wait_timeout_ms(unsigned int ms) {
+  unsigned long long v = ms ? (unsigned long long)ms : 4000ull;
+  g_timeout_ns.store(v * 1000ull * 1000ull);
+}
+
+int uaa_check_device_status(uaa_stream_t stream) {
+  DevCtx ctx;
+  int st = get_dev_ctx(&ctx);
+  if (st != UAA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word) {
+    e = cudaMemset(ctx.status, 0, sizeof(unsigned int));
+    if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "status clear sync: %s", cudaGetErrorString(e));
+  }
+  if (word & kStatusTimeout)
+    return set_error(UAA_ERR_TIMEOUT, "a bounded device-side wait ran out (status word 0x%x)", word);
+  return UAA_OK;
+}
+
+int uaa_watchdog_selftest(unsigned int timeout_us, uaa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000)
+    return set_error(UAA_ERR_INVALID_ARG, "uaa_watchdog_selftest: timeout_us must be in [1, 1000000]");
+  DevCtx ctx;
+  int st = get_dev_ctx(&ctx);
+  if (st != UAA_OK) return st;
+  ctx.timeout_ns = (unsigned long long)timeout_us * 1000ull;
+  watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctx);
+  return check_launch("uaa_watchdog_selftest");
+}
+
+}  // extern "C"
