@@ -19,6 +19,7 @@ CPU oracle on bounded samples of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -214,6 +215,14 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.workload(WORKLOAD)
+    workload_name = WORKLOAD
+    if args.heads:
+        # smaller-head variant of the same workload (same launch shapes per head group),
+        # used to keep ncu captures small
+        if args.heads % w.P:
+            raise SystemExit("--heads must be a multiple of P=4")
+        w = dataclasses.replace(w, H=args.heads)
+        workload_name = f"ulysses_p4_n27280_h{args.heads}_d128"
     B, S, H, D, P = w.B, w.S, w.H, w.D, w.P
     lens, cap, Hg = w.shard_lens, w.cap, w.H // w.P
     inp = synth.make(w)
@@ -347,7 +356,7 @@ def run_gpu(args, world, rank, local):
         "metric": "attention fwd+bwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "N": S, "P": P, "H": H, "D": D, "shard_lens": list(lens),
+        "config": {"workload": workload_name, "B": B, "N": S, "P": P, "H": H, "D": D, "shard_lens": list(lens),
                    "cap": cap, "mask": None, "l2": "inputs larger than L2 (4 x 279 MB shards), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU, 4 emulated Ulysses ranks"},
         "parts_ms_per_step": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms, "relayout": relayout_ms},
@@ -372,6 +381,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--heads", type=int, default=0, help="override H (profiling-size variant)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "uaa" else args.warmup
     if args.impl == "reference":

@@ -27,8 +27,15 @@ def bits(t):
     return t.view(torch.uint8).numpy()
 
 
-def compare(name, got, ref, kind=None):
-    """Assert the acceptance bar; returns (max_abs, rel_fro)."""
+def compare(name, got, ref, kind=None, magnitude_scaled=False):
+    """Assert the acceptance bar; returns (max_abs, rel_fro).
+
+    The max-abs bars are stated for the workloads (N(0,1) inputs, scale 1/sqrt(D)),
+    whose outputs are O(1).  With ``magnitude_scaled`` (used for a non-default
+    softmax scale, where outputs grow to several units and one bf16 ULP alone is
+    ~0.03) the max-abs bar is multiplied by max(1, max|ref|): the same relative
+    accuracy.  The relative Frobenius bar is unchanged.
+    """
     kind = kind or name
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -41,7 +48,10 @@ def compare(name, got, ref, kind=None):
     max_abs = float(err.max()) if err.size else 0.0
     nrm = float(np.linalg.norm(ref[fin]))
     rel = float(np.linalg.norm(got[fin] - ref[fin]) / nrm) if nrm > 0 else float(np.linalg.norm(got[fin]))
-    assert max_abs <= TOL_MAX_ABS[kind], f"{name}: max-abs {max_abs:.3e} > {TOL_MAX_ABS[kind]}"
+    bar = TOL_MAX_ABS[kind]
+    if magnitude_scaled and fin.any():
+        bar *= max(1.0, float(np.abs(ref[fin]).max()))
+    assert max_abs <= bar, f"{name}: max-abs {max_abs:.3e} > {bar:.3e}"
     if nrm > 0:
         assert rel <= TOL_REL_FRO, f"{name}: rel-Frobenius {rel:.3e} > {TOL_REL_FRO}"
     return max_abs, rel
