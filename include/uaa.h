@@ -97,6 +97,37 @@ int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                  void* dq, void* dk, void* dv, int B, int S, int H, int D, float scale,
                  void* workspace, size_t workspace_bytes, uaa_stream_t stream);
 
+/* Allocation-free variant of uaa_attn_bwd.  The source pages have no
+ * counterpart; this entry point exists for callers that cannot allocate device
+ * memory when they run the backward -- code running inside an allocator
+ * callback, plugins that may only enqueue work on a stream they were handed,
+ * runtimes whose device allocations are all planned up front, latency-bound
+ * loops that must not take the allocator's locks -- and so cannot provide the
+ * workspace uaa_attn_bwd asks for.
+ *
+ * It computes exactly what uaa_attn_bwd computes (same arguments minus the
+ * workspace) but uses a scratch array built into the library: a file-scope
+ * device array of uaa_attn_bwd_noalloc_max_bytes() bytes (64 MiB), which every
+ * GPU that loads the library holds until the process exits.  Requests whose
+ * uaa_attn_bwd_workspace_bytes(B, S, H, D) exceeds that size are rejected
+ * with UAA_ERR_UNSUPPORTED (use uaa_attn_bwd instead).  The call itself never
+ * allocates or frees device memory.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture begins.
+ *  - All calls share the one array, which keeps the last call's contents.
+ *    Calls whose kernels may overlap on the GPU (e.g. on two streams with no
+ *    ordering between them) race on it and produce wrong gradients; order
+ *    them on one stream or with events.
+ *  - Every call re-initialises the parts that must start at zero. */
+int uaa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                         const void* dout, const float* lse, const uint8_t* key_mask,
+                         void* dq, void* dk, void* dv, int B, int S, int H, int D, float scale,
+                         uaa_stream_t stream);
+
+/* Size in bytes of the scratch array used by uaa_attn_bwd_noalloc. */
+size_t uaa_attn_bwd_noalloc_max_bytes(void);
+
 /* Ulysses forward exchange on one device: sequence shards -> head groups.
  * "UAA-bwd", What does this PR do (all-to-all with saved partition metadata,
  * uneven shards); "fast-ulysses", Summary (A2A around the attention module).

@@ -49,6 +49,8 @@ _SIGS = {
     "uaa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "uaa_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P,
                           ctypes.c_size_t, _P]),
+    "uaa_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "uaa_attn_bwd_noalloc_max_bytes": (ctypes.c_size_t, []),
     "uaa_seq_to_head": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "uaa_head_to_seq": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "uaa_assemble_key_mask": (_I, [_P, _P, _I, _P, _I, _I, _P]),

@@ -28,6 +28,8 @@
 // [256+D,256+2D) dK.
 #include <math.h>
 
+#include <mutex>
+
 #include "uaa_common.cuh"
 
 namespace uaa {
@@ -618,4 +620,73 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
                                           s, ctx)
                   : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, acc,
                                            s, ctx);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the backward.
+//
+// Some callers cannot call cudaMalloc at the point where they run the backward:
+// code inside a custom allocator callback, a plugin that may only launch work
+// on a stream it was handed, a runtime that has pre-planned every device
+// allocation and forbids new ones, or a latency-bound loop that must not take
+// the allocator's locks.  They cannot size and hand over the workspace that
+// uaa_attn_bwd asks for, so this entry point uses a fixed scratch array that
+// lives in the library itself.
+//
+// The array is a file-scope device variable: every GPU that loads the library
+// holds kNoAllocScratchBytes of it until the process exits.  Host code cannot
+// use the array's name as a device address, so the first call on each device
+// looks the address up (cudaGetSymbolAddress, with that device current) and
+// caches it; make that first call before any stream capture begins.  All calls
+// share the one array: two calls whose kernels overlap on the GPU (different
+// streams, no ordering between them) race on it and give wrong results.
+// Nothing in the array needs to start at zero: the Delta part is fully written
+// and the dQ accumulator is zeroed by the preprocess kernel of every call.
+namespace uaa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB
+__device__ __align__(256) uint8_t g_bwd_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+int scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return set_error(UAA_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+    if (e != cudaSuccess)
+      return set_error(UAA_ERR_CUDA, "cudaGetSymbolAddress(backward scratch): %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return UAA_OK;
+}
+
+}  // namespace
+}  // namespace uaa
+
+extern "C" size_t uaa_attn_bwd_noalloc_max_bytes(void) { return uaa::kNoAllocScratchBytes; }
+
+extern "C" int uaa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                    const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int B,
+                                    int S, int H, int D, float scale, uaa_stream_t stream) {
+  const char* fn = "uaa_attn_bwd_noalloc";
+  int st = validate_attn_sizes(fn, B, S, H, D, scale);
+  if (st) return st;
+  if ((uint64_t)B * S * H == 0) return UAA_OK;
+  const size_t need = uaa_attn_bwd_workspace_bytes(B, S, H, D);
+  if (need > kNoAllocScratchBytes)
+    return set_error(UAA_ERR_UNSUPPORTED,
+                     "%s: B*S*H*D too large for the built-in scratch (%zu bytes needed, %zu available); "
+                     "use uaa_attn_bwd with a caller-provided workspace",
+                     fn, need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((st = scratch_address(&scratch))) return st;
+  return uaa_attn_bwd(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, D, scale, scratch, need, stream);
 }
