@@ -18,7 +18,8 @@
 //        dV  += P^T dO         (TMEM accumulator, A = P^T from shared memory)
 //        dK  += dS^T Q         (TMEM accumulator, A = dS^T from shared memory)
 //        dQ_i = dS K           (TMEM, A = the same dS^T buffer read MN-major)
-//     dQ_i is added to the fp32 accumulator with 16-byte atomics.
+//     The fp32 dQ_i tile is staged in shared memory and added to the
+//     accumulator with TMA tensor reduce-adds.
 //     warp 8 = TMA producer, warp 9 = tcgen05 issuer, warps 0-7 = compute
 //     (thread = key row; warps 0-3 take query columns 0-63, warps 4-7 64-127).
 //     Keys outside the mask get P = 0, hence dK = dV = 0 exactly; a key tile
@@ -42,6 +43,9 @@ namespace {
 constexpr int kBK = 128;  // keys per CTA (TMEM lanes)
 constexpr int kBQ = 128;  // queries per inner tile
 constexpr int kChunkBytes = 128 * 128;
+constexpr int kComputeThreads = 256;  // warps 0-7
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 
 template <int D>
@@ -53,14 +57,14 @@ struct BwdLayout {
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kDO = kQ + kQStages * kTileBytes;
-  static constexpr int kPT = kDO + kDStages * kTileBytes;
-  static constexpr int kDST = kPT + kBK * kBQ * 2;
-  static constexpr int kLse = kDST + kBK * kBQ * 2;
+  static constexpr int kPDS = kDO + kDStages * kTileBytes;          // P^T, then dS^T, then half the dQ staging
+  static constexpr int kSTG = kPDS + kBK * kBQ * 2;                 // the other half of the fp32 dQ staging
+  static constexpr int kLse = kSTG + kBQ * (D / 2) * 4;
   static constexpr int kDelta = kLse + kQStages * kBQ * 4;
-  static constexpr int kCtl = kDelta + kDStages * kBQ * 4;
-  static constexpr int kBytes = kCtl + 256;
-  static constexpr int kSmem = kBytes + 1024;
+  static constexpr int kCtl = kDelta + kQStages * kBQ * 4;
+  static constexpr int kSmem = kCtl + 256;
   static_assert(kSmem <= 232448, "backward shared memory exceeds the per-CTA limit");
+  static_assert(kBQ * (D / 2) * 4 <= kBK * kBQ * 2, "dQ staging half must fit the P/dS buffer");
 };
 
 struct BwdCtl {
@@ -69,16 +73,21 @@ struct BwdCtl {
   uint64_t bar_q_empty[2];
   uint64_t bar_do_full[2];
   uint64_t bar_do_empty[2];
-  uint64_t bar_s;
-  uint64_t bar_dp;
+  uint64_t bar_s_full;
+  uint64_t bar_dp_full;
+  uint64_t bar_p_ready;
+  uint64_t bar_dv_done;
   uint64_t bar_ds_ready;
-  uint64_t bar_dq;
+  uint64_t bar_dq_full;
   uint64_t bar_dq_free;
+  uint64_t bar_pds_free;
+  uint64_t bar_staged;
   uint64_t bar_kv_done;
   uint64_t bar_final;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(BwdCtl) <= 256, "control block");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -198,30 +207,46 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
 
 // ---------------------------------------------------------------------------
 // 2. main backward kernel
+//
+// Per query tile i the tensor core runs, in this order,
+//   dP^T_i = V dO_i^T             (TMEM columns [128,256))
+//   dV    += P^T_i dO_i           (A = P^T in the shared P/dS buffer)
+//   dK    += dS^T_i Q_i           (A = dS^T in the same buffer, after dV is done)
+//   dQ_i   = dS_i K               (A = dS^T read MN-major; into the dP^T columns)
+//   S^T_{i+1} = K Q_{i+1}^T       (TMEM columns [0,128))
+// so S^T_{i+1} runs while the compute warps read dQ_i out of TMEM, and the
+// fp32 dQ partial tile leaves through shared memory with TMA reduce-adds
+// (cp.reduce.async.bulk.tensor ... .add) instead of per-thread atomics.
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const float* __restrict__ lse, const float* __restrict__ delta,
-                    const uint8_t* __restrict__ key_mask, float* __restrict__ dq_acc,
+                    const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ lse,
+                    const float* __restrict__ delta, const uint8_t* __restrict__ key_mask,
                     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int S, int H, float scale,
                     float scale_log2, DevCtx ctx) {
   using L = BwdLayout<D>;
   constexpr int kChunks = D / 64;
   constexpr int QST = L::kQStages;
   constexpr int DST = L::kDStages;
+  constexpr int kBoxes = D / 32;  // 32-column fp32 boxes of the dQ tile
   constexpr uint32_t kIdescKK = idesc_bf16_f32(128, kBQ, false, false);  // S^T, dP^T
   constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV, dK
   constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);      // dQ
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   BwdCtl* ctl = reinterpret_cast<BwdCtl*>(smem + L::kCtl);
   float* sLse = reinterpret_cast<float*>(smem + L::kLse);
   float* sDelta = reinterpret_cast<float*>(smem + L::kDelta);
   const uint32_t sbase = smem_u32(smem);
 
+  if (sbase & 1023u) {
+    // the swizzled operand tiles need 1024-byte alignment; never expected to trigger
+    if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadLaunch);
+    return;
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kt = blockIdx.x;
@@ -260,23 +285,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->bar_do_full[s], 1);
       mbar_init(&ctl->bar_do_empty[s], 1);
     }
-    mbar_init(&ctl->bar_s, 1);
-    mbar_init(&ctl->bar_dp, 1);
-    mbar_init(&ctl->bar_ds_ready, 8 * 32);
-    mbar_init(&ctl->bar_dq, 1);
-    mbar_init(&ctl->bar_dq_free, 8 * 32);
+    mbar_init(&ctl->bar_s_full, 1);
+    mbar_init(&ctl->bar_dp_full, 1);
+    mbar_init(&ctl->bar_p_ready, kComputeThreads);
+    mbar_init(&ctl->bar_dv_done, 1);
+    mbar_init(&ctl->bar_ds_ready, kComputeThreads);
+    mbar_init(&ctl->bar_dq_full, 1);
+    mbar_init(&ctl->bar_dq_free, kComputeThreads);
+    mbar_init(&ctl->bar_pds_free, 1);
+    mbar_init(&ctl->bar_staged, kComputeThreads);
     mbar_init(&ctl->bar_kv_done, 1);
     mbar_init(&ctl->bar_final, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmAcc);
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, 512);
     tmem_relinquish();
   }
@@ -289,8 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t do_armed[2] = {0, 0};
   bool kv_armed = false;
   bool mma_issued = false;
+  bool bulk_issued = false;
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
     if (lane == 0) {
@@ -319,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (l != -INFINITY) l2 = l * kLog2e;
         }
         sLse[qs * kBQ + 32 * t + lane] = l2;
+        sDelta[qs * kBQ + 32 * t + lane] = q < S ? delta_bh[q] : 0.f;
       }
       __syncwarp();
       if (lane == 0) {
@@ -334,12 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int q = i * kBQ + 32 * t + lane;
-        sDelta[ds * kBQ + 32 * t + lane] = q < S ? delta_bh[q] : 0.f;
-      }
-      __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes);
 #pragma unroll
@@ -349,22 +375,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         do_armed[ds] = du + 1;
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = wait_or_abort(&ctl->bar_kv, 0, ctx, ctl);
-      tc_fence_after();
       const uint32_t sK = sbase + L::kK;
       const uint32_t sV = sbase + L::kV;
-      const uint32_t sPT = sbase + L::kPT;
-      const uint32_t sDST = sbase + L::kDST;
-      for (int i = 0; ok && i < nqt; ++i) {
+      const uint32_t sPDS = sbase + L::kPDS;
+      auto issue_s = [&](int i) -> bool {
         const int qs = i % QST;
-        const int ds = i % DST;
-        const uint32_t sQ = sbase + L::kQ + qs * L::kTileBytes;
-        const uint32_t sDO = sbase + L::kDO + ds * L::kTileBytes;
-        if (!(ok = wait_or_abort(&ctl->bar_q_full[qs], (i / QST) & 1, ctx, ctl))) break;
+        if (!wait_or_abort(&ctl->bar_q_full[qs], (i / QST) & 1, ctx, ctl)) return false;
         tc_fence_after();
+        const uint32_t sQ = sbase + L::kQ + qs * L::kTileBytes;
         // S^T = K Q^T  (M = keys, N = queries, K = D; both K-major)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -372,9 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), kIdescKK,
                    kk > 0);
         }
-        mma_commit(&ctl->bar_s);
+        mma_commit(&ctl->bar_s_full);
         mma_issued = true;
-        // dP^T = V dO^T  (into the columns dQ_{i-1} used: wait until it was read)
+        return true;
+      };
+      bool ok = wait_or_abort(&ctl->bar_kv, 0, ctx, ctl);
+      tc_fence_after();
+      if (ok) ok = issue_s(0);
+      for (int i = 0; ok && i < nqt; ++i) {
+        const int qs = i % QST;
+        const int ds = i % DST;
+        const uint32_t sQ = sbase + L::kQ + qs * L::kTileBytes;
+        const uint32_t sDO = sbase + L::kDO + ds * L::kTileBytes;
+        // dP^T = V dO^T into the columns dQ_{i-1} used: wait until it was read out
         if (i > 0) {
           if (!(ok = wait_or_abort(&ctl->bar_dq_free, (i - 1) & 1, ctx, ctl))) break;
           tc_fence_after();
@@ -387,52 +418,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), kIdescKK,
                    kk > 0);
         }
-        mma_commit(&ctl->bar_dp);
-        // P^T and dS^T are in shared memory
-        if (!(ok = wait_or_abort(&ctl->bar_ds_ready, i & 1, ctx, ctl))) break;
+        mma_commit(&ctl->bar_dp_full);
+        // dV += P^T dO  (A = P^T, K-major over queries; B = dO MN-major)
+        if (!(ok = wait_or_abort(&ctl->bar_p_ready, i & 1, ctx, ctl))) break;
         tc_fence_after();
-        // dV += P^T dO  (A K-major over queries, B = dO MN-major)
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColDV, sdesc_sw128(sPT + aoff, 16, 1024),
+          mma_bf16(tmem + kColDV, sdesc_sw128(sPDS + aoff, 16, 1024),
                    sdesc_sw128(sDO + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&ctl->bar_do_empty[ds]);
-        // dK += dS^T Q  (A K-major over queries, B = Q MN-major)
+        mma_commit(&ctl->bar_dv_done);
+        // dK += dS^T Q  (A = dS^T, K-major over queries; B = Q MN-major)
+        if (!(ok = wait_or_abort(&ctl->bar_ds_ready, i & 1, ctx, ctl))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColDK, sdesc_sw128(sDST + aoff, 16, 1024),
+          mma_bf16(tmem + kColDK, sdesc_sw128(sPDS + aoff, 16, 1024),
                    sdesc_sw128(sQ + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&ctl->bar_q_empty[qs]);
-        // dQ_i = dS K  (A = dS^T buffer read MN-major: M = queries, K = keys; B = K MN-major)
+        // dQ_i = dS K  (A = dS^T read MN-major: M = queries, K = keys; B = K MN-major)
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          mma_bf16(tmem + kColDP, sdesc_sw128(sDST + kk * 2048, kChunkBytes, 1024),
+          mma_bf16(tmem + kColDP, sdesc_sw128(sPDS + kk * 2048, kChunkBytes, 1024),
                    sdesc_sw128(sK + kk * 2048, kChunkBytes, 1024), kIdescMM, kk > 0);
         }
-        mma_commit(&ctl->bar_dq);
+        mma_commit(&ctl->bar_dq_full);
+        // S^T of the next tile (its columns were freed when P_i was formed)
+        if (i + 1 < nqt && !(ok = issue_s(i + 1))) break;
       }
       if (ok) mma_commit(&ctl->bar_kv_done);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps 0..7
+    const int ctid = threadIdx.x;  // 0..255
     const int qd = warp & 3;
     const int hf = warp >> 2;
-    const int jrow = qd * 32 + lane;  // key row of this thread (TMEM lane)
+    const int jrow = qd * 32 + lane;  // key row (TMEM lane) in the S^T / dP^T phase; query row for dQ
     const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
     const int key = k0 + jrow;
     const bool kvalid = key < S && (!kMask || key_mask[(size_t)b * S + key] != 0);
-    uint8_t* sPTc = smem + L::kPT + hf * kChunkBytes;
-    uint8_t* sDSTc = smem + L::kDST + hf * kChunkBytes;
+    uint8_t* sPDSc = smem + L::kPDS + hf * kChunkBytes;
+    // fp32 dQ staging: boxes [0, kBoxes/2) in the staging buffer, the rest in the P/dS buffer
+    uint8_t* stg = hf == 0 ? smem + L::kSTG : smem + L::kPDS;
     bool ok = true;
     for (int i = 0; i < nqt; ++i) {
       const int qs = i % QST;
-      const int ds = i % DST;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s, i & 1, ctx, ctl));
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, i & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
       float p[64];
@@ -440,44 +476,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tl + kColS + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(&p[32]));
       ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[qs], (i / QST) & 1, ctx, ctl));
       if (!ok) break;
-      const float* l2 = sLse + qs * kBQ + 64 * hf;
+      {
+        const float4* l2 = reinterpret_cast<const float4*>(sLse + qs * kBQ + 64 * hf);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) p[c] = kvalid ? ex2(fmaf(p[c], scale_log2, -l2[c])) : 0.f;
-      store_row_chunk_sw128(sPTc, jrow, p);
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp, i & 1, ctx, ctl));
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = l2[c4];
+          p[4 * c4 + 0] = kvalid ? ex2(fmaf(p[4 * c4 + 0], scale_log2, -l.x)) : 0.f;
+          p[4 * c4 + 1] = kvalid ? ex2(fmaf(p[4 * c4 + 1], scale_log2, -l.y)) : 0.f;
+          p[4 * c4 + 2] = kvalid ? ex2(fmaf(p[4 * c4 + 2], scale_log2, -l.z)) : 0.f;
+          p[4 * c4 + 3] = kvalid ? ex2(fmaf(p[4 * c4 + 3], scale_log2, -l.w)) : 0.f;
+        }
+      }
+      if (i > 0) {
+        // the P/dS buffer also held the previous dQ staging: its TMA reads must be done
+        if (ctid == 0) {
+          bulk_wait_read_all();
+          mbar_arrive(&ctl->bar_pds_free);
+        }
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pds_free, (i - 1) & 1, ctx, ctl));
+        if (!ok) break;
+      }
+      store_row_chunk_sw128(sPDSc, jrow, p);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ctl->bar_p_ready);
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp_full, i & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
       float dp[64];
       tmem_ld32(tl + kColDP + 64 * hf, *reinterpret_cast<float(*)[32]>(&dp[0]));
       tmem_ld32(tl + kColDP + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(&dp[32]));
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_do_full[ds], (i / DST) & 1, ctx, ctl));
-      if (!ok) break;
-      const float* dl = sDelta + ds * kBQ + 64 * hf;
+      {
+        // Delta_i sits with the Q_i stage (q_full was waited on above)
+        const float4* dl = reinterpret_cast<const float4*>(sDelta + qs * kBQ + 64 * hf);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) dp[c] = p[c] * (dp[c] - dl[c]);
-      store_row_chunk_sw128(sDSTc, jrow, dp);
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 d = dl[c4];
+          dp[4 * c4 + 0] = p[4 * c4 + 0] * (dp[4 * c4 + 0] - d.x);
+          dp[4 * c4 + 1] = p[4 * c4 + 1] * (dp[4 * c4 + 1] - d.y);
+          dp[4 * c4 + 2] = p[4 * c4 + 2] * (dp[4 * c4 + 2] - d.z);
+          dp[4 * c4 + 3] = p[4 * c4 + 3] * (dp[4 * c4 + 3] - d.w);
+        }
+      }
+      // P^T must have been consumed by the dV MMA before dS^T overwrites it
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dv_done, i & 1, ctx, ctl));
+      if (!ok) break;
+      store_row_chunk_sw128(sPDSc, jrow, dp);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&ctl->bar_ds_ready);
-      // dQ_i: TMEM lane = query row of tile i, this half of the D columns
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dq, i & 1, ctx, ctl));
+      // dQ_i: TMEM lane = query row of tile i; this thread takes columns [hf*D/2, (hf+1)*D/2)
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dq_full, i & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
-      const int q = i * kBQ + jrow;
-      float4* dst = reinterpret_cast<float4*>(dq_acc + (((size_t)b * S + q) * H + h) * D + hf * (D / 2));
-#pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
-        float g[32];
-        tmem_ld32(tl + kColDP + hf * (D / 2) + 32 * c, g);
-        if (q < S) {
+      float g[D / 2];
 #pragma unroll
-          for (int t = 0; t < 8; ++t)
-            atomicAdd(dst + 8 * c + t, make_float4(g[4 * t], g[4 * t + 1], g[4 * t + 2], g[4 * t + 3]));
-        }
-      }
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(tl + kColDP + hf * (D / 2) + 32 * c, *reinterpret_cast<float(*)[32]>(&g[32 * c]));
       tc_fence_before();
       mbar_arrive(&ctl->bar_dq_free);
+      // stage the fp32 partial tile (128-byte swizzled boxes of 32 columns) and reduce-add it
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx) {
+        uint8_t* box = stg + bx * (kBQ * 128);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float* src = &g[32 * bx + 4 * c4];
+          *reinterpret_cast<float4*>(box + jrow * 128 + ((c4 ^ (jrow & 7)) << 4)) =
+              make_float4(src[0], src[1], src[2], src[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ctl->bar_staged);
+      if (warp == 0) {
+        bool staged = true;
+        if (lane == 0) staged = wait_or_abort(&ctl->bar_staged, i & 1, ctx, ctl);
+        ok = __all_sync(0xffffffffu, staged);
+        if (!ok) break;
+      }
+      if (ctid == 0) {
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          const uint8_t* box = (bx < kBoxes / 2 ? smem + L::kSTG : smem + L::kPDS) + (bx % (kBoxes / 2)) * (kBQ * 128);
+          tma_reduce_add_4d(box, &tmAcc, 32 * bx, h, i * kBQ, b);
+        }
+        bulk_commit_group();
+        bulk_issued = true;
+      }
     }
+    if (ctid == 0 && bulk_issued) bulk_wait_all();  // the reductions have landed before the kernel ends
     if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_kv_done, 0, ctx, ctl));
     if (ok) {
       tc_fence_after();
@@ -516,11 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 9 && lane == 0 && mma_issued) {
+  if (warp == kMmaWarp && lane == 0 && mma_issued) {
     mma_commit(&ctl->bar_final);
     settle(&ctl->bar_final, 0, ctx);
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     if (kv_armed) settle(&ctl->bar_kv, 0, ctx);
     for (int s = 0; s < 2; ++s) {
       if (q_armed[s]) settle(&ctl->bar_q_full[s], (q_armed[s] - 1) & 1, ctx);
@@ -529,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -554,17 +641,18 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
       reinterpret_cast<float4*>(acc), B, S, H, acc_vec4);
   int st = check_launch("uaa_attn_bwd (preprocess)");
   if (st) return st;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, macc;
   if ((st = encode_bshd_map(&mq, q, B, S, H, D, 128))) return st;
   if ((st = encode_bshd_map(&mk, k, B, S, H, D, 128))) return st;
   if ((st = encode_bshd_map(&mv, v, B, S, H, D, 128))) return st;
   if ((st = encode_bshd_map(&mdo, dout, B, S, H, D, 128))) return st;
+  if ((st = encode_bshd_map_f32(&macc, acc, B, S, H, D, 128))) return st;
   auto kern = attn_bwd_kernel<D, kMask>;
   const int smem = BwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
   dim3 grid((S + kBK - 1) / kBK, H, B);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, lse, delta, mask, acc, static_cast<__nv_bfloat16*>(dk),
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, lse, delta, mask, static_cast<__nv_bfloat16*>(dk),
                                          static_cast<__nv_bfloat16*>(dv), S, H, scale, scale * kLog2e, ctx);
   if ((st = check_launch("uaa_attn_bwd (main)"))) return st;
   const size_t n8 = rows * D / 8;

@@ -64,7 +64,8 @@ int get_dev_ctx(DevCtx* ctx) {
   return UAA_OK;
 }
 
-int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows) {
+// The driver's tensor-map encoder, resolved once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -73,7 +74,11 @@ int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int 
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
-  if (!g_encode) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return g_encode;
+}
+
+int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows) {
+  if (!encoder()) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   // dims innermost first: D (contiguous), H, S, B; a box is 64 elements of D
   // (one 128-byte swizzle row) x 1 head x box_rows positions x 1 batch.
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
@@ -84,6 +89,19 @@ int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int 
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return UAA_OK;
+}
+
+int encode_bshd_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows) {
+  if (!encoder()) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4, (cuuint64_t)S * H * D * 4};
+  cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (CUresult %d)", (int)r);
   return UAA_OK;
 }
 
@@ -131,6 +149,8 @@ int uaa_check_device_status(uaa_stream_t stream) {
   }
   if (word & kStatusTimeout)
     return set_error(UAA_ERR_TIMEOUT, "a bounded device-side wait ran out (status word 0x%x)", word);
+  if (word & kStatusBadLaunch)
+    return set_error(UAA_ERR_CUDA, "a kernel refused its launch configuration (status word 0x%x)", word);
   return UAA_OK;
 }
 

@@ -19,7 +19,8 @@ namespace uaa {
 // uaa_check_device_status() reads and clears).
 // ----------------------------------------------------------------------------
 enum : uint32_t {
-  kStatusTimeout = 1u,
+  kStatusTimeout = 1u,      // a bounded wait ran out
+  kStatusBadLaunch = 2u,    // a kernel refused its launch configuration (e.g. misaligned shared memory)
 };
 
 struct DevCtx {
@@ -32,6 +33,8 @@ int get_dev_ctx(DevCtx* ctx);           // returns UAA_OK or UAA_ERR_CUDA (messa
 int set_error(int status, const char* fmt, ...);
 int check_launch(const char* what);     // cudaGetLastError -> UAA_ERR_CUDA
 int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows);
+// fp32 (B, S, H, D) tensor; box = 32 columns (128 bytes) x box_rows positions, 128-byte swizzle.
+int encode_bshd_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows);
 
 #if defined(__CUDACC__)
 
@@ -105,6 +108,24 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+
+// 4-D tiled tensor reduce-add from shared memory into global memory (bulk-group
+// completion; out-of-range rows of the box are not written).
+__device__ __forceinline__ void tma_reduce_add_4d(const void* smem_src, const CUtensorMap* map, int c0, int c1,
+                                                  int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
