@@ -75,15 +75,16 @@ int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key
                  void* out, float* lse, int B, int S, int H, int D, float scale,
                  uaa_stream_t stream);
 
-/* Bytes of device workspace uaa_attn_bwd needs for (B, S, H, D):
- * an fp32 (B, H, S) row-dot vector Delta = rowsum(dO * O) followed (at a
- * 256-byte aligned offset) by an fp32 (B, S, H, D) dQ accumulator.
+/* Bytes of device workspace uaa_attn_bwd needs for (B, S, H, D): the fp32
+ * (B, H, S) row-dot vector Delta = rowsum(dO * O), rounded up to 256 bytes.
  * Returns 0 for invalid sizes. */
 size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D);
 
 /* Attention backward: dQ, dK, dV from dO, O and LSE.
  * "double-transpose", description: the backward op receives Q, K, V in one
  * layout (no second transpose of K/V), dO in BSHD and the saved LSE.
+ * The result is deterministic (no atomics): two calls on the same inputs give
+ * identical bits.
  *   q, k, v, out, dout : device, bf16 (B, S, H, D)
  *   lse                : device, fp32 (B, H, S), as written by uaa_attn_fwd
  *   key_mask           : device, uint8 (B, S) or NULL; must be the mask the

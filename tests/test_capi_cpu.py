@@ -36,8 +36,7 @@ def test_exports_every_declared_symbol(L):
 def test_workspace_bytes(L):
     B, S, H, D = 1, 27280, 40, 128
     got = L.uaa_attn_bwd_workspace_bytes(B, S, H, D)
-    delta = (B * H * S * 4 + 255) // 256 * 256
-    assert got == delta + B * S * H * D * 4
+    assert got == (B * H * S * 4 + 255) // 256 * 256  # the fp32 Delta vector only
     assert L.uaa_attn_bwd_workspace_bytes(1, 16, 2, 96) == 0
 
 

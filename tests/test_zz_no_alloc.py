@@ -60,7 +60,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     L = uaa.lib()
     cap = L.uaa_attn_bwd_noalloc_max_bytes()
     assert cap == 64 << 20
-    B, S, H, D = 1, 27280, 10, 128
+    B, S, H, D = 16, 27280, 40, 128
     assert L.uaa_attn_bwd_workspace_bytes(B, S, H, D) > cap
     fake = ctypes.c_void_p(1 << 20)
     st = L.uaa_attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, B, S, H, D,

@@ -8,25 +8,31 @@
 // differentiated; the backward of each head group is the plain attention
 // backward.
 //
-// Three kernels:
-//  1. bwd_preprocess_kernel: Delta_i = sum_d dO_id * O_id (fp32), equal to
-//     sum_j P_ij dP_ij, and zeroes the fp32 dQ accumulator.
-//  2. attn_bwd_kernel: one CTA per 128-key tile of one (batch, head), looping
-//     over all 128-row query tiles (K/V-tile-major):
-//        S^T  = K Q^T          (TMEM, M = keys)        P^T = exp2(S^T*c - lse2)
-//        dP^T = V dO^T         (TMEM)                  dS^T = P^T (dP^T - Delta)
-//        dV  += P^T dO         (TMEM accumulator, A = P^T from shared memory)
-//        dK  += dS^T Q         (TMEM accumulator, A = dS^T from shared memory)
-//        dQ_i = dS K           (TMEM, A = the same dS^T buffer read MN-major)
-//     The fp32 dQ_i tile is staged in shared memory and added to the
-//     accumulator with TMA tensor reduce-adds.
-//     warp 8 = TMA producer, warp 9 = tcgen05 issuer, warps 0-7 = compute
-//     (thread = key row; warps 0-3 take query columns 0-63, warps 4-7 64-127).
-//     Keys outside the mask get P = 0, hence dK = dV = 0 exactly; a key tile
-//     with no attended key writes zeros and skips all work.
-//  3. dq_convert_kernel: dQ = bf16(scale * accumulator).
-// TMEM columns: [0,128) S^T, [128,256) dP^T then dQ, [256,256+D) dV,
-// [256+D,256+2D) dK.
+// Three kernels, no atomics and no reductions, so every gradient is
+// deterministic:
+//  1. bwd_preprocess_kernel: Delta_i = sum_d dO_id * O_id (fp32), which equals
+//     sum_j P_ij dP_ij.
+//  2. attn_bwd_dkdv_kernel (K/V-tile-major): a persistent CTA takes a 128-key
+//     tile of one (batch, head) and loops over all 128-row query tiles:
+//        S^T  = K Q^T,  P^T = exp2(S^T*c - lse2)            (M = keys)
+//        dP^T = V dO^T, dS^T = P^T (dP^T - Delta)
+//        dV  += P^T dO, dK += dS^T Q                        (accumulated in TMEM)
+//     P^T and dS^T are written back to TMEM as bf16 and read from there as
+//     the A operand of the dV / dK MMAs.
+//  3. attn_bwd_dq_kernel (Q-tile-major): a persistent CTA takes a 128-row
+//     query tile and loops over the key tiles, recomputing S = Q K^T and
+//     dP = dO V^T with Q and dO held in TMEM as A operands (so these MMAs
+//     read only K / V from shared memory); dS = P (dP - Delta) goes back to
+//     TMEM as bf16 and dQ += dS K accumulates in TMEM; dQ is written once,
+//     in bf16.  The extra S / dP recomputation (7 GEMMs instead of 5 for the
+//     whole backward) buys a reduction-free, deterministic dQ.
+// Keys outside the mask get P = 0, hence dK = dV = 0 exactly; key tiles with
+// no attended key are skipped (the dK/dV kernel writes zeros for them).
+//
+// Warp roles in both main kernels: warps 0-7 compute (TMEM lane quadrant =
+// warp % 4, column half = warp / 4), warp 8 TMA producer, warp 9 tcgen05
+// issuer.  An MMA that overwrites TMEM columns an earlier MMA of the same
+// thread reads is issued after it: the MMAs of one thread execute in order.
 #include <math.h>
 
 #include <mutex>
@@ -40,54 +46,12 @@ int check_dev_ptr(const char* fn, const char* name, const void* p);
 
 namespace {
 
-constexpr int kBK = 128;  // keys per CTA (TMEM lanes)
-constexpr int kBQ = 128;  // queries per inner tile
+constexpr int kBT = 128;  // rows per query tile and per key tile
 constexpr int kChunkBytes = 128 * 128;
 constexpr int kComputeThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
-
-template <int D>
-struct BwdLayout {
-  static constexpr int kQStages = 2;
-  static constexpr int kDStages = (D == 128) ? 1 : 2;
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;
-  static constexpr int kDO = kQ + kQStages * kTileBytes;
-  static constexpr int kPDS = kDO + kDStages * kTileBytes;          // P^T, then dS^T, then half the dQ staging
-  static constexpr int kSTG = kPDS + kBK * kBQ * 2;                 // the other half of the fp32 dQ staging
-  static constexpr int kLse = kSTG + kBQ * (D / 2) * 4;
-  static constexpr int kDelta = kLse + kQStages * kBQ * 4;
-  static constexpr int kCtl = kDelta + kQStages * kBQ * 4;
-  static constexpr int kSmem = kCtl + 256;
-  static_assert(kSmem <= 232448, "backward shared memory exceeds the per-CTA limit");
-  static_assert(kBQ * (D / 2) * 4 <= kBK * kBQ * 2, "dQ staging half must fit the P/dS buffer");
-};
-
-struct BwdCtl {
-  uint64_t bar_kv;
-  uint64_t bar_q_full[2];
-  uint64_t bar_q_empty[2];
-  uint64_t bar_do_full[2];
-  uint64_t bar_do_empty[2];
-  uint64_t bar_s_full;
-  uint64_t bar_dp_full;
-  uint64_t bar_p_ready;
-  uint64_t bar_dv_done;
-  uint64_t bar_ds_ready;
-  uint64_t bar_dq_full;
-  uint64_t bar_dq_free;
-  uint64_t bar_pds_free;
-  uint64_t bar_staged;
-  uint64_t bar_kv_done;
-  uint64_t bar_final;
-  uint32_t tmem_base;
-  int abort;
-};
-static_assert(sizeof(BwdCtl) <= 256, "control block");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -100,7 +64,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const DevCtx& ctx, BwdCtl* ctl) {
+template <typename Ctl>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const DevCtx& ctx, Ctl* ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -125,36 +90,65 @@ __device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity, const Dev
   if (!mbar_wait(bar, parity, ctx.timeout_ns)) atomicOr(ctx.status, kStatusTimeout);
 }
 
-// Write 64 consecutive values of row `row` as bf16 into a 128-byte-swizzled
-// K-major tile chunk (128 rows x 64 columns).
-__device__ __forceinline__ void store_row_chunk_sw128(uint8_t* chunk, int row, const float (&x)[64]) {
+// Warp-collective: the attended-key bits of key tile j (bit c of word t = key
+// 128j + 32t + c); keys past S count as masked.  Every lane gets all 4 words.
+__device__ __forceinline__ void key_tile_bits(const uint8_t* __restrict__ key_mask, int b, int S, int j,
+                                              uint32_t (&w)[4]) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int pc = 0; pc < 8; ++pc) {
-    uint4 v;
-    v.x = pack_bf16(x[pc * 8 + 0], x[pc * 8 + 1]);
-    v.y = pack_bf16(x[pc * 8 + 2], x[pc * 8 + 3]);
-    v.z = pack_bf16(x[pc * 8 + 4], x[pc * 8 + 5]);
-    v.w = pack_bf16(x[pc * 8 + 6], x[pc * 8 + 7]);
-    *reinterpret_cast<uint4*>(chunk + row * 128 + ((pc ^ (row & 7)) << 4)) = v;
+  for (int t = 0; t < 4; ++t) {
+    const int key = j * kBT + 32 * t + lane;
+    const bool valid = key < S && (key_mask == nullptr || key_mask[(size_t)b * S + key] != 0);
+    w[t] = __ballot_sync(0xffffffffu, valid);
   }
 }
 
+__device__ __forceinline__ bool key_tile_any(const uint8_t* __restrict__ key_mask, int b, int S, int j) {
+  uint32_t w[4];
+  key_tile_bits(key_mask, b, S, j, w);
+  return (w[0] | w[1] | w[2] | w[3]) != 0;
+}
+
+// Packed bf16 pairs of 64 consecutive columns -> 32 TMEM columns (two stores).
+__device__ __forceinline__ void store_packed64(uint32_t taddr, const float (&x)[64]) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(x[2 * c], x[2 * c + 1]);
+  tmem_st32_bits(taddr, pk);
+}
+
+struct Item3 {
+  int t, h, b;
+};
+__device__ __forceinline__ Item3 decode_item(int item, int ntiles, int H) {
+  Item3 it;
+  it.t = item % ntiles;
+  const int bh = item / ntiles;
+  it.h = bh % H;
+  it.b = bh / H;
+  return it;
+}
+
+// TMEM column of the A operand for K step kk (16 elements = 8 packed columns)
+// when the 128 packed K elements sit as two runs of 32 columns at base and
+// base + 64 (column half hf of the compute warps writes its 64 elements into
+// the first 32 columns of its own 64-column region).
+__device__ __forceinline__ uint32_t packed_a_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+
 // ---------------------------------------------------------------------------
-// 1. Delta = rowsum(dO * O); zero the dQ accumulator.
-// Eight lanes per (b, s, h) row, 16-byte loads; Delta stored as (B, H, S).
+// 1. Delta = rowsum(dO * O).  Eight lanes per (b, s, h) row, 16-byte loads;
+// stored as (B, H, S).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
-                                                             float* __restrict__ delta, float4* __restrict__ dq_acc,
-                                                             int B, int S, int H, size_t acc_vec4) {
-  constexpr int kVecPerRow = D / 8;        // 16-byte vectors per row
-  constexpr int kPerLane = kVecPerRow / 8;  // vectors per lane (8 lanes per row)
+                                                             float* __restrict__ delta, int B, int S, int H) {
+  constexpr int kVecPerRow = D / 8;
+  constexpr int kPerLane = kVecPerRow / 8;
   const size_t rows = (size_t)B * S * H;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t nthreads = (size_t)gridDim.x * blockDim.x;
   const int sub = threadIdx.x & 7;
-  for (size_t base = tid >> 3; base < ((rows + 3) / 4) * 4; base += nthreads >> 3) {
-    const size_t r = base;
+  for (size_t r = tid >> 3; r < ((rows + 3) / 4) * 4; r += nthreads >> 3) {
     float acc = 0.f;
     if (r < rows) {
       const uint4* po = reinterpret_cast<const uint4*>(o + r * D);
@@ -185,63 +179,56 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       delta[((size_t)b * H + h) * S + s] = acc;
     }
   }
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (size_t i = tid; i < acc_vec4; i += nthreads) dq_acc[i] = z;
 }
 
 // ---------------------------------------------------------------------------
-// 3. dQ = bf16(scale * accumulator), 8 elements per thread.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
-                                                         float scale, size_t n8) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = __ldcs(acc + 2 * i);
-    const float4 c = __ldcs(acc + 2 * i + 1);
-    uint4 v;
-    v.x = pack_bf16(a.x * scale, a.y * scale);
-    v.y = pack_bf16(a.z * scale, a.w * scale);
-    v.z = pack_bf16(c.x * scale, c.y * scale);
-    v.w = pack_bf16(c.z * scale, c.w * scale);
-    dq[i] = v;
-  }
-}
+// 2. dK / dV (K/V-tile-major)
+template <int D>
+struct DkdvLayout {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQStages = 3;                   // Q_i (+ Delta_i): last read by dK_i
+  static constexpr int kDStages = 2;                   // dO_i (+ -LSE*log2e): last read by dV_i
+  static constexpr int kQ = kV + kTileBytes;
+  static constexpr int kDO = kQ + kQStages * kTileBytes;
+  static constexpr int kLse = kDO + kDStages * kTileBytes;
+  static constexpr int kDelta = kLse + kDStages * kBT * 4;
+  static constexpr int kCtl = kDelta + kQStages * kBT * 4;
+  static constexpr int kSmem = kCtl + 256;
+  static_assert(kSmem <= 232448, "dK/dV shared memory exceeds the per-CTA limit");
+};
 
-// ---------------------------------------------------------------------------
-// 2. main backward kernel
-//
-// Per query tile i the tensor core runs, in this order,
-//   dP^T_i = V dO_i^T             (TMEM columns [128,256))
-//   dV    += P^T_i dO_i           (A = P^T in the shared P/dS buffer)
-//   dK    += dS^T_i Q_i           (A = dS^T in the same buffer, after dV is done)
-//   dQ_i   = dS_i K               (A = dS^T read MN-major; into the dP^T columns)
-//   S^T_{i+1} = K Q_{i+1}^T       (TMEM columns [0,128))
-// so S^T_{i+1} runs while the compute warps read dQ_i out of TMEM, and the
-// fp32 dQ partial tile leaves through shared memory with TMA reduce-adds
-// (cp.reduce.async.bulk.tensor ... .add) instead of per-thread atomics.
+struct DkdvCtl {
+  uint64_t bar_kv_full, bar_kv_empty;
+  uint64_t bar_q_full[3], bar_q_empty[3];
+  uint64_t bar_do_full[2], bar_do_empty[2];
+  uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready;
+  uint64_t bar_acc_done, bar_acc_free, bar_final;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(DkdvCtl) <= 256, "control block");
+
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ lse,
-                    const float* __restrict__ delta, const uint8_t* __restrict__ key_mask,
-                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int S, int H, float scale,
-                    float scale_log2, DevCtx ctx) {
-  using L = BwdLayout<D>;
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                         const float* __restrict__ lse, const float* __restrict__ delta,
+                         const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ dk,
+                         __nv_bfloat16* __restrict__ dv, int S, int H, int num_items, float scale,
+                         float scale_log2, DevCtx ctx) {
+  using L = DkdvLayout<D>;
   constexpr int kChunks = D / 64;
-  constexpr int QST = L::kQStages;
-  constexpr int DST = L::kDStages;
-  constexpr int kBoxes = D / 32;  // 32-column fp32 boxes of the dQ tile
-  constexpr uint32_t kIdescKK = idesc_bf16_f32(128, kBQ, false, false);  // S^T, dP^T
-  constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV, dK
-  constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);      // dQ
+  constexpr uint32_t kIdescKK = idesc_bf16_f32(128, kBT, false, false);  // S^T, dP^T
+  constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV, dK (A in TMEM)
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw;
-  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(smem + L::kCtl);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  DkdvCtl* ctl = reinterpret_cast<DkdvCtl*>(smem + L::kCtl);
   float* sLse = reinterpret_cast<float*>(smem + L::kLse);
   float* sDelta = reinterpret_cast<float*>(smem + L::kDelta);
   const uint32_t sbase = smem_u32(smem);
-
   if (sbase & 1023u) {
     // the swizzled operand tiles need 1024-byte alignment; never expected to trigger
     if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadLaunch);
@@ -249,52 +236,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kt = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int k0 = kt * kBK;
-  const int nqt = (S + kBQ - 1) / kBQ;
-
-  if (kMask) {
-    // A key tile without any attended key contributes nothing: dK = dV = 0.
-    int valid = 0;
-    if (threadIdx.x < kBK) {
-      const int key = k0 + threadIdx.x;
-      valid = key < S && key_mask[(size_t)b * S + key] != 0;
-    }
-    if (!__syncthreads_or(valid)) {
-      constexpr int kVec = D / 8;
-      for (int idx = threadIdx.x; idx < kBK * kVec; idx += kThreads) {
-        const int r = idx / kVec;
-        const int c = idx % kVec;
-        if (k0 + r < S) {
-          const size_t off = (((size_t)b * S + k0 + r) * H + h) * D + c * 8;
-          *reinterpret_cast<uint4*>(dk + off) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(dv + off) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      return;
-    }
-  }
+  const int nkt = (S + kBT - 1) / kBT;
+  const int nqt = nkt;
+  const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
-    mbar_init(&ctl->bar_kv, 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(&ctl->bar_kv_full, 1);
+    mbar_init(&ctl->bar_kv_empty, 1);
+    for (int s = 0; s < L::kQStages; ++s) {
       mbar_init(&ctl->bar_q_full[s], 1);
       mbar_init(&ctl->bar_q_empty[s], 1);
+    }
+    for (int s = 0; s < L::kDStages; ++s) {
       mbar_init(&ctl->bar_do_full[s], 1);
       mbar_init(&ctl->bar_do_empty[s], 1);
     }
     mbar_init(&ctl->bar_s_full, 1);
     mbar_init(&ctl->bar_dp_full, 1);
     mbar_init(&ctl->bar_p_ready, kComputeThreads);
-    mbar_init(&ctl->bar_dv_done, 1);
     mbar_init(&ctl->bar_ds_ready, kComputeThreads);
-    mbar_init(&ctl->bar_dq_full, 1);
-    mbar_init(&ctl->bar_dq_free, kComputeThreads);
-    mbar_init(&ctl->bar_pds_free, 1);
-    mbar_init(&ctl->bar_staged, kComputeThreads);
-    mbar_init(&ctl->bar_kv_done, 1);
+    mbar_init(&ctl->bar_acc_done, 1);
+    mbar_init(&ctl->bar_acc_free, kComputeThreads);
     mbar_init(&ctl->bar_final, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -304,7 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
-    tma_prefetch_desc(&tmAcc);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, 512);
@@ -315,288 +276,269 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  uint32_t q_armed[2] = {0, 0};
-  uint32_t do_armed[2] = {0, 0};
-  bool kv_armed = false;
+  uint32_t q_armed[3] = {0, 0, 0}, do_armed[2] = {0, 0}, kv_armed = 0;
   bool mma_issued = false;
-  bool bulk_issued = false;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&ctl->bar_kv, 2 * L::kTileBytes);
+    uint32_t nq = 0, it = 0;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+      const Item3 w = decode_item(item, nkt, H);
+      if (kMask && !key_tile_any(mask, w.b, S, w.t)) continue;
+      if (lane == 0) {
+        if (it > 0) ok = wait_or_abort(&ctl->bar_kv_empty, (it - 1) & 1, ctx, ctl);
+        if (ok) {
+          mbar_arrive_expect_tx(&ctl->bar_kv_full, 2 * L::kTileBytes);
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        tma_load_4d(smem + L::kK + c * kChunkBytes, &tmK, &ctl->bar_kv, c * 64, h, k0, b);
-        tma_load_4d(smem + L::kV + c * kChunkBytes, &tmV, &ctl->bar_kv, c * 64, h, k0, b);
-      }
-      kv_armed = true;
-    }
-    const float* lse_bh = lse + ((size_t)b * H + h) * S;
-    const float* delta_bh = delta + ((size_t)b * H + h) * S;
-    for (int i = 0; i < nqt; ++i) {
-      const int qs = i % QST;
-      const uint32_t qu = i / QST;
-      if (lane == 0 && qu > 0) ok = wait_or_abort(&ctl->bar_q_empty[qs], (qu - 1) & 1, ctx, ctl);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int q = i * kBQ + 32 * t + lane;
-        float l2 = INFINITY;  // rows past the end, and fully masked rows, get P = 0
-        if (q < S) {
-          const float l = lse_bh[q];
-          if (l != -INFINITY) l2 = l * kLog2e;
+          for (int c = 0; c < kChunks; ++c) {
+            tma_load_4d(smem + L::kK + c * kChunkBytes, &tmK, &ctl->bar_kv_full, c * 64, w.h, w.t * kBT, w.b);
+            tma_load_4d(smem + L::kV + c * kChunkBytes, &tmV, &ctl->bar_kv_full, c * 64, w.h, w.t * kBT, w.b);
+          }
+          kv_armed = it + 1;
         }
-        sLse[qs * kBQ + 32 * t + lane] = l2;
-        sDelta[qs * kBQ + 32 * t + lane] = q < S ? delta_bh[q] : 0.f;
       }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&ctl->bar_q_full[qs], L::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(smem + L::kQ + qs * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full[qs], c * 64, h,
-                      i * kBQ, b);
-        q_armed[qs] = qu + 1;
-      }
-      const int ds = i % DST;
-      const uint32_t du = i / DST;
-      if (lane == 0 && du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes);
+      const float* lse_bh = lse + ((size_t)w.b * H + w.h) * S;
+      const float* delta_bh = delta + ((size_t)w.b * H + w.h) * S;
+      for (int i = 0; ok && i < nqt; ++i, ++nq) {
+        const int qs = nq % L::kQStages;
+        const uint32_t qu = nq / L::kQStages;
+        const int ds = nq % L::kDStages;
+        const uint32_t du = nq / L::kDStages;
+        if (lane == 0 && qu > 0) ok = wait_or_abort(&ctl->bar_q_empty[qs], (qu - 1) & 1, ctx, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(smem + L::kDO + ds * L::kTileBytes + c * kChunkBytes, &tmDO, &ctl->bar_do_full[ds], c * 64,
-                      h, i * kBQ, b);
-        do_armed[ds] = du + 1;
+        for (int t = 0; t < 4; ++t) {
+          const int q = i * kBT + 32 * t + lane;
+          sDelta[qs * kBT + 32 * t + lane] = q < S ? delta_bh[q] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->bar_q_full[qs], L::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(smem + L::kQ + qs * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full[qs], c * 64,
+                        w.h, i * kBT, w.b);
+          q_armed[qs] = qu + 1;
+          if (du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int q = i * kBT + 32 * t + lane;
+          float nl2 = -INFINITY;  // -LSE*log2(e): rows past the end and fully masked rows get P = 0
+          if (q < S) {
+            const float l = lse_bh[q];
+            if (l != -INFINITY) nl2 = -l * kLog2e;
+          }
+          sLse[ds * kBT + 32 * t + lane] = nl2;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(smem + L::kDO + ds * L::kTileBytes + c * kChunkBytes, &tmDO, &ctl->bar_do_full[ds], c * 64,
+                        w.h, i * kBT, w.b);
+          do_armed[ds] = du + 1;
+        }
       }
+      ++it;
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sK = sbase + L::kK;
-      const uint32_t sV = sbase + L::kV;
-      const uint32_t sPDS = sbase + L::kPDS;
-      auto issue_s = [&](int i) -> bool {
-        const int qs = i % QST;
-        if (!wait_or_abort(&ctl->bar_q_full[qs], (i / QST) & 1, ctx, ctl)) return false;
-        tc_fence_after();
-        const uint32_t sQ = sbase + L::kQ + qs * L::kTileBytes;
-        // S^T = K Q^T  (M = keys, N = queries, K = D; both K-major)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), kIdescKK,
-                   kk > 0);
-        }
-        mma_commit(&ctl->bar_s_full);
-        mma_issued = true;
-        return true;
-      };
-      bool ok = wait_or_abort(&ctl->bar_kv, 0, ctx, ctl);
-      tc_fence_after();
-      if (ok) ok = issue_s(0);
-      for (int i = 0; ok && i < nqt; ++i) {
-        const int qs = i % QST;
-        const int ds = i % DST;
-        const uint32_t sQ = sbase + L::kQ + qs * L::kTileBytes;
-        const uint32_t sDO = sbase + L::kDO + ds * L::kTileBytes;
-        // dP^T = V dO^T into the columns dQ_{i-1} used: wait until it was read out
-        if (i > 0) {
-          if (!(ok = wait_or_abort(&ctl->bar_dq_free, (i - 1) & 1, ctx, ctl))) break;
+    // ------------------------------------------------------------ MMA issuer (lane 0 issues)
+    bool ok = true;
+    uint32_t nq = 0, it = 0;
+    const uint32_t sK = sbase + L::kK;
+    const uint32_t sV = sbase + L::kV;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+      const Item3 w = decode_item(item, nkt, H);
+      if (kMask && !key_tile_any(mask, w.b, S, w.t)) continue;
+      if (lane == 0) {
+        auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
+        auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
+        auto issue_s = [&](uint32_t g) -> bool {
+          if (!wait_or_abort(&ctl->bar_q_full[g % L::kQStages], (g / L::kQStages) & 1, ctx, ctl)) return false;
           tc_fence_after();
-        }
-        if (!(ok = wait_or_abort(&ctl->bar_do_full[ds], (i / DST) & 1, ctx, ctl))) break;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            mma_bf16(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sq(g) + off, 16, 1024), kIdescKK,
+                     kk > 0);
+          }
+          mma_commit(&ctl->bar_s_full);
+          return true;
+        };
+        auto issue_dp = [&](uint32_t g) -> bool {
+          if (!wait_or_abort(&ctl->bar_do_full[g % L::kDStages], (g / L::kDStages) & 1, ctx, ctl)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            mma_bf16(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdo(g) + off, 16, 1024),
+                     kIdescKK, kk > 0);
+          }
+          mma_commit(&ctl->bar_dp_full);
+          return true;
+        };
+        ok = wait_or_abort(&ctl->bar_kv_full, it & 1, ctx, ctl);
         tc_fence_after();
+        if (ok) ok = issue_s(nq);
+        if (ok) ok = issue_dp(nq);
+        mma_issued = true;
+        for (int i = 0; ok && i < nqt; ++i) {
+          const uint32_t g = nq + i;
+          // dV += P^T dO  (A = P^T in the S^T columns)
+          if (!(ok = wait_or_abort(&ctl->bar_p_ready, g & 1, ctx, ctl))) break;
+          tc_fence_after();
+          if (i == 0 && it > 0) {
+            // the previous item's epilogue must have read dK / dV
+            if (!(ok = wait_or_abort(&ctl->bar_acc_free, (it - 1) & 1, ctx, ctl))) break;
+            tc_fence_after();
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), kIdescKK,
-                   kk > 0);
-        }
-        mma_commit(&ctl->bar_dp_full);
-        // dV += P^T dO  (A = P^T, K-major over queries; B = dO MN-major)
-        if (!(ok = wait_or_abort(&ctl->bar_p_ready, i & 1, ctx, ctl))) break;
-        tc_fence_after();
+          for (int kk = 0; kk < kBT / 16; ++kk)
+            mma_bf16_ts(tmem + kColDV, tmem + kColS + packed_a_col(kk),
+                        sdesc_sw128(sdo(g) + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl->bar_do_empty[g % L::kDStages]);
+          // S^T of the next tile (P^T was read by the dV MMAs just issued)
+          if (i + 1 < nqt && !(ok = issue_s(g + 1))) break;
+          // dK += dS^T Q  (A = dS^T in the dP^T columns)
+          if (!(ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBQ / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColDV, sdesc_sw128(sPDS + aoff, 16, 1024),
-                   sdesc_sw128(sDO + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBT / 16; ++kk)
+            mma_bf16_ts(tmem + kColDK, tmem + kColDP + packed_a_col(kk),
+                        sdesc_sw128(sq(g) + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&ctl->bar_q_empty[g % L::kQStages]);
+          // dP^T of the next tile (dS^T was read by the dK MMAs just issued)
+          if (i + 1 < nqt && !(ok = issue_dp(g + 1))) break;
         }
-        mma_commit(&ctl->bar_do_empty[ds]);
-        mma_commit(&ctl->bar_dv_done);
-        // dK += dS^T Q  (A = dS^T, K-major over queries; B = Q MN-major)
-        if (!(ok = wait_or_abort(&ctl->bar_ds_ready, i & 1, ctx, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBQ / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColDK, sdesc_sw128(sPDS + aoff, 16, 1024),
-                   sdesc_sw128(sQ + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+        if (ok) {
+          mma_commit(&ctl->bar_acc_done);
+          mma_commit(&ctl->bar_kv_empty);
         }
-        mma_commit(&ctl->bar_q_empty[qs]);
-        // dQ_i = dS K  (A = dS^T read MN-major: M = queries, K = keys; B = K MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          mma_bf16(tmem + kColDP, sdesc_sw128(sPDS + kk * 2048, kChunkBytes, 1024),
-                   sdesc_sw128(sK + kk * 2048, kChunkBytes, 1024), kIdescMM, kk > 0);
-        }
-        mma_commit(&ctl->bar_dq_full);
-        // S^T of the next tile (its columns were freed when P_i was formed)
-        if (i + 1 < nqt && !(ok = issue_s(i + 1))) break;
       }
-      if (ok) mma_commit(&ctl->bar_kv_done);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      nq += nqt;
+      ++it;
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps 0..7
-    const int ctid = threadIdx.x;  // 0..255
     const int qd = warp & 3;
     const int hf = warp >> 2;
-    const int jrow = qd * 32 + lane;  // key row (TMEM lane) in the S^T / dP^T phase; query row for dQ
+    const int jrow = qd * 32 + lane;  // key row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
-    const int key = k0 + jrow;
-    const bool kvalid = key < S && (!kMask || key_mask[(size_t)b * S + key] != 0);
-    uint8_t* sPDSc = smem + L::kPDS + hf * kChunkBytes;
-    // fp32 dQ staging: boxes [0, kBoxes/2) in the staging buffer, the rest in the P/dS buffer
-    uint8_t* stg = hf == 0 ? smem + L::kSTG : smem + L::kPDS;
     bool ok = true;
-    for (int i = 0; i < nqt; ++i) {
-      const int qs = i % QST;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, i & 1, ctx, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      float p[64];
-      tmem_ld32(tl + kColS + 64 * hf, *reinterpret_cast<float(*)[32]>(&p[0]));
-      tmem_ld32(tl + kColS + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(&p[32]));
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[qs], (i / QST) & 1, ctx, ctl));
-      if (!ok) break;
-      {
-        const float4* l2 = reinterpret_cast<const float4*>(sLse + qs * kBQ + 64 * hf);
+    uint32_t nq = 0, it = 0;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+      const Item3 w = decode_item(item, nkt, H);
+      const int key = w.t * kBT + jrow;
+      if (kMask && !key_tile_any(mask, w.b, S, w.t)) {
+        // no attended key in this tile: dK = dV = 0
+        if (key < S) {
+          const size_t off = (((size_t)w.b * S + key) * H + w.h) * D + hf * (D / 2);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l = l2[c4];
-          p[4 * c4 + 0] = kvalid ? ex2(fmaf(p[4 * c4 + 0], scale_log2, -l.x)) : 0.f;
-          p[4 * c4 + 1] = kvalid ? ex2(fmaf(p[4 * c4 + 1], scale_log2, -l.y)) : 0.f;
-          p[4 * c4 + 2] = kvalid ? ex2(fmaf(p[4 * c4 + 2], scale_log2, -l.z)) : 0.f;
-          p[4 * c4 + 3] = kvalid ? ex2(fmaf(p[4 * c4 + 3], scale_log2, -l.w)) : 0.f;
+          for (int c = 0; c < D / 16; ++c) {
+            *reinterpret_cast<uint4*>(dk + off + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dv + off + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
+        continue;
       }
-      if (i > 0) {
-        // the P/dS buffer also held the previous dQ staging: its TMA reads must be done
-        if (ctid == 0) {
-          bulk_wait_read_all();
-          mbar_arrive(&ctl->bar_pds_free);
-        }
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pds_free, (i - 1) & 1, ctx, ctl));
+      const bool kvalid = key < S && (!kMask || key_mask[(size_t)w.b * S + key] != 0);
+      for (int i = 0; i < nqt; ++i) {
+        const uint32_t g = nq + i;
+        const int qs = g % L::kQStages;
+        const int ds = g % L::kDStages;
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, g & 1, ctx, ctl));
         if (!ok) break;
-      }
-      store_row_chunk_sw128(sPDSc, jrow, p);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ctl->bar_p_ready);
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp_full, i & 1, ctx, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      float dp[64];
-      tmem_ld32(tl + kColDP + 64 * hf, *reinterpret_cast<float(*)[32]>(&dp[0]));
-      tmem_ld32(tl + kColDP + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(&dp[32]));
-      {
-        // Delta_i sits with the Q_i stage (q_full was waited on above)
-        const float4* dl = reinterpret_cast<const float4*>(sDelta + qs * kBQ + 64 * hf);
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 d = dl[c4];
-          dp[4 * c4 + 0] = p[4 * c4 + 0] * (dp[4 * c4 + 0] - d.x);
-          dp[4 * c4 + 1] = p[4 * c4 + 1] * (dp[4 * c4 + 1] - d.y);
-          dp[4 * c4 + 2] = p[4 * c4 + 2] * (dp[4 * c4 + 2] - d.z);
-          dp[4 * c4 + 3] = p[4 * c4 + 3] * (dp[4 * c4 + 3] - d.w);
-        }
-      }
-      // P^T must have been consumed by the dV MMA before dS^T overwrites it
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dv_done, i & 1, ctx, ctl));
-      if (!ok) break;
-      store_row_chunk_sw128(sPDSc, jrow, dp);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ctl->bar_ds_ready);
-      // dQ_i: TMEM lane = query row of tile i; this thread takes columns [hf*D/2, (hf+1)*D/2)
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dq_full, i & 1, ctx, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      float g[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tmem_ld32(tl + kColDP + hf * (D / 2) + 32 * c, *reinterpret_cast<float(*)[32]>(&g[32 * c]));
-      tc_fence_before();
-      mbar_arrive(&ctl->bar_dq_free);
-      // stage the fp32 partial tile (128-byte swizzled boxes of 32 columns) and reduce-add it
-#pragma unroll
-      for (int bx = 0; bx < D / 64; ++bx) {
-        uint8_t* box = stg + bx * (kBQ * 128);
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float* src = &g[32 * bx + 4 * c4];
-          *reinterpret_cast<float4*>(box + jrow * 128 + ((c4 ^ (jrow & 7)) << 4)) =
-              make_float4(src[0], src[1], src[2], src[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&ctl->bar_staged);
-      if (warp == 0) {
-        bool staged = true;
-        if (lane == 0) staged = wait_or_abort(&ctl->bar_staged, i & 1, ctx, ctl);
-        ok = __all_sync(0xffffffffu, staged);
+        tc_fence_after();
+        float p[64];
+        tmem_ld32x2(tl + kColS + 64 * hf, tl + kColS + 64 * hf + 32, p);
+        // -LSE*log2e of Q_i sits with the dO_i stage, Delta_i with the Q_i stage
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_do_full[ds], (g / L::kDStages) & 1, ctx, ctl));
         if (!ok) break;
-      }
-      if (ctid == 0) {
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[qs], (g / L::kQStages) & 1, ctx, ctl));
+        if (!ok) break;
+        {
+          const float2* nl2 = reinterpret_cast<const float2*>(sLse + ds * kBT + 64 * hf);
+          const float2 c2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-        for (int bx = 0; bx < kBoxes; ++bx) {
-          const uint8_t* box = (bx < kBoxes / 2 ? smem + L::kSTG : smem + L::kPDS) + (bx % (kBoxes / 2)) * (kBQ * 128);
-          tma_reduce_add_4d(box, &tmAcc, 32 * bx, h, i * kBQ, b);
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = fma2(make_float2(p[2 * c], p[2 * c + 1]), c2, nl2[c]);
+            p[2 * c] = ex2(x.x);
+            p[2 * c + 1] = ex2(x.y);
+          }
+          if (!kvalid) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) p[c] = 0.f;
+          }
         }
-        bulk_commit_group();
-        bulk_issued = true;
+        // P^T as bf16 over the first 32 columns of this half's S^T region
+        store_packed64(tl + kColS + 64 * hf, p);
+        tc_fence_before();
+        mbar_arrive(&ctl->bar_p_ready);
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp_full, g & 1, ctx, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        float dp[64];
+        tmem_ld32x2(tl + kColDP + 64 * hf, tl + kColDP + 64 * hf + 32, dp);
+        {
+          const float2* dl = reinterpret_cast<const float2*>(sDelta + qs * kBT + 64 * hf);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 d =
+                mul2(make_float2(p[2 * c], p[2 * c + 1]), sub2(make_float2(dp[2 * c], dp[2 * c + 1]), dl[c]));
+            dp[2 * c] = d.x;
+            dp[2 * c + 1] = d.y;
+          }
+        }
+        store_packed64(tl + kColDP + 64 * hf, dp);
+        tc_fence_before();
+        mbar_arrive(&ctl->bar_ds_ready);
       }
-    }
-    if (ctid == 0 && bulk_issued) bulk_wait_all();  // the reductions have landed before the kernel ends
-    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_kv_done, 0, ctx, ctl));
-    if (ok) {
+      if (!ok) break;
+      // epilogue: dV, and dK = scale * (dS^T Q)
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_acc_done, it & 1, ctx, ctl));
+      if (!ok) break;
       tc_fence_after();
-      const size_t off = (((size_t)b * S + key) * H + h) * D + hf * (D / 2);
+      const size_t off = (((size_t)w.b * S + key) * H + w.h) * D + hf * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
-        float g[32];
-        tmem_ld32(tl + kColDV + hf * (D / 2) + 32 * c, g);
+        float gg[32];
+        tmem_ld32(tl + kColDV + hf * (D / 2) + 32 * c, gg);
         if (key < S) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
-            v.x = pack_bf16(g[8 * t + 0], g[8 * t + 1]);
-            v.y = pack_bf16(g[8 * t + 2], g[8 * t + 3]);
-            v.z = pack_bf16(g[8 * t + 4], g[8 * t + 5]);
-            v.w = pack_bf16(g[8 * t + 6], g[8 * t + 7]);
+            v.x = pack_bf16(gg[8 * t + 0], gg[8 * t + 1]);
+            v.y = pack_bf16(gg[8 * t + 2], gg[8 * t + 3]);
+            v.z = pack_bf16(gg[8 * t + 4], gg[8 * t + 5]);
+            v.w = pack_bf16(gg[8 * t + 6], gg[8 * t + 7]);
             *reinterpret_cast<uint4*>(dv + off + 32 * c + 8 * t) = v;
           }
         }
-        tmem_ld32(tl + kColDK + hf * (D / 2) + 32 * c, g);
+        tmem_ld32(tl + kColDK + hf * (D / 2) + 32 * c, gg);
         if (key < S) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
-            v.x = pack_bf16(g[8 * t + 0] * scale, g[8 * t + 1] * scale);
-            v.y = pack_bf16(g[8 * t + 2] * scale, g[8 * t + 3] * scale);
-            v.z = pack_bf16(g[8 * t + 4] * scale, g[8 * t + 5] * scale);
-            v.w = pack_bf16(g[8 * t + 6] * scale, g[8 * t + 7] * scale);
+            v.x = pack_bf16(gg[8 * t + 0] * scale, gg[8 * t + 1] * scale);
+            v.y = pack_bf16(gg[8 * t + 2] * scale, gg[8 * t + 3] * scale);
+            v.z = pack_bf16(gg[8 * t + 4] * scale, gg[8 * t + 5] * scale);
+            v.w = pack_bf16(gg[8 * t + 6] * scale, gg[8 * t + 7] * scale);
             *reinterpret_cast<uint4*>(dk + off + 32 * c + 8 * t) = v;
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&ctl->bar_acc_free);
+      nq += nqt;
+      ++it;
     }
   }
 
@@ -608,11 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     settle(&ctl->bar_final, 0, ctx);
   }
   if (warp == kProducerWarp && lane == 0) {
-    if (kv_armed) settle(&ctl->bar_kv, 0, ctx);
-    for (int s = 0; s < 2; ++s) {
+    if (kv_armed) settle(&ctl->bar_kv_full, (kv_armed - 1) & 1, ctx);
+    for (int s = 0; s < 3; ++s)
       if (q_armed[s]) settle(&ctl->bar_q_full[s], (q_armed[s] - 1) & 1, ctx);
+    for (int s = 0; s < 2; ++s)
       if (do_armed[s]) settle(&ctl->bar_do_full[s], (do_armed[s] - 1) & 1, ctx);
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -622,47 +564,411 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// 3. dQ (Q-tile-major)
+template <int D>
+struct DqLayout {
+  static constexpr int kRing = (D == 128) ? 6 : 8;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kRingOff = 0;  // K_j, V_j, K_j+1, ... (Q and dO live in TMEM)
+  static constexpr int kCtl = kRingOff + kRing * kTileBytes;
+  static constexpr int kSmem = kCtl + 512;
+  static_assert(kSmem <= 232448, "dQ shared memory exceeds the per-CTA limit");
+};
+
+struct DqCtl {
+  uint64_t bar_qdo_ready;
+  uint64_t bar_kv_full[8], bar_kv_empty[8];
+  uint64_t bar_s_full, bar_s_read, bar_dp_full, bar_ds_ready;
+  uint64_t bar_dq_done, bar_dq_free, bar_final;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(DqCtl) <= 512, "control block");
+
+template <int D, bool kMask>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const float* __restrict__ lse, const float* __restrict__ delta,
+                       const uint8_t* __restrict__ key_mask, const __nv_bfloat16* __restrict__ qg,
+                       const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int S, int H,
+                       int num_items, float scale, float scale_log2, DevCtx ctx) {
+  using L = DqLayout<D>;
+  constexpr int kChunks = D / 64;
+  constexpr int R = L::kRing;
+  constexpr uint32_t kIdescKK = idesc_bf16_f32(128, kBT, false, false);  // S, dP
+  constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dQ (A in TMEM)
+  // TMEM: S, dP (then dS), the dQ accumulator, and Q / dO as A operands of S / dP
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 384, kColDO = 448;
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  DqCtl* ctl = reinterpret_cast<DqCtl*>(smem + L::kCtl);
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadLaunch);
+    return;
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nkt = (S + kBT - 1) / kBT;
+  const int nqt = nkt;
+  const uint8_t* mask = kMask ? key_mask : nullptr;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->bar_qdo_ready, kComputeThreads);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(&ctl->bar_kv_full[s], 1);
+      mbar_init(&ctl->bar_kv_empty[s], 1);
+    }
+    mbar_init(&ctl->bar_s_full, 1);
+    mbar_init(&ctl->bar_s_read, kComputeThreads);
+    mbar_init(&ctl->bar_dp_full, 1);
+    mbar_init(&ctl->bar_ds_ready, kComputeThreads);
+    mbar_init(&ctl->bar_dq_done, 1);
+    mbar_init(&ctl->bar_dq_free, kComputeThreads);
+    mbar_init(&ctl->bar_final, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  uint32_t kv_armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  bool mma_issued = false;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    uint32_t n = 0, it = 0;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+      const Item3 w = decode_item(item, nqt, H);
+      for (int j = 0; ok && j < nkt; ++j) {
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
+        if (kMask) {
+          key_tile_bits(mask, w.b, S, j, words);
+          if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
+        }
+#pragma unroll
+        for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
+          const int slot = n % R;
+          const uint32_t use = n / R;
+          if (lane == 0 && use > 0) ok = wait_or_abort(&ctl->bar_kv_empty[slot], (use - 1) & 1, ctx, ctl);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
+            const CUtensorMap* map = kind == 0 ? &tmK : &tmV;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + c * kChunkBytes, map,
+                          &ctl->bar_kv_full[slot], c * 64, w.h, j * kBT, w.b);
+            kv_armed[slot] = use + 1;
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (lane 0 issues)
+    bool ok = true;
+    uint32_t g = 0, it = 0;  // g: processed key tiles across items
+    auto ring = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+      const Item3 w = decode_item(item, nqt, H);
+      // the key tiles of this item, in order (all lanes evaluate the same mask)
+      int j = 0;
+      auto next_tile = [&](int from) {
+        for (int jj = from; jj < nkt; ++jj)
+          if (!kMask || key_tile_any(mask, w.b, S, jj)) return jj;
+        return nkt;
+      };
+      bool first = true;
+      // Q and dO of this item were stored into TMEM by the compute warps
+      if (lane == 0) ok = wait_or_abort(&ctl->bar_qdo_ready, it & 1, ctx, ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      j = next_tile(0);
+      auto issue_s = [&](uint32_t gg) -> bool {
+        const uint32_t nk = 2 * gg;
+        if (!wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, sdesc_sw128(ring(nk) + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(&ctl->bar_s_full);
+        return true;
+      };
+      auto issue_dp = [&](uint32_t gg) -> bool {
+        const uint32_t nv = 2 * gg + 1;
+        if (!wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, sdesc_sw128(ring(nv) + off, 16, 1024), kIdescKK,
+                      kk > 0);
+        }
+        mma_commit(&ctl->bar_dp_full);
+        mma_commit(&ctl->bar_kv_empty[nv % R]);  // V_j is only read by this dP
+        return true;
+      };
+      if (j < nkt) {
+        if (lane == 0) {
+          ok = issue_s(g);
+          if (ok) ok = issue_dp(g);
+          mma_issued = true;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      while (ok && j < nkt) {
+        const int jn = next_tile(j + 1);
+        if (lane == 0) {
+          // S of the next key tile once this one's S was read into registers
+          if (jn < nkt) {
+            ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
+            if (ok) {
+              tc_fence_after();
+              ok = issue_s(g + 1);
+            }
+          }
+          // dQ += dS K_j  (A = dS in the dP columns)
+          if (ok) ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl);
+          if (ok && first && it > 0) ok = wait_or_abort(&ctl->bar_dq_free, (it - 1) & 1, ctx, ctl);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t nk = 2 * g;
+#pragma unroll
+            for (int kk = 0; kk < kBT / 16; ++kk)
+              mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk),
+                          sdesc_sw128(ring(nk) + kk * 2048, kChunkBytes, 1024), kIdescKM,
+                          (!first || kk > 0) ? 1u : 0u);
+            mma_commit(&ctl->bar_kv_empty[nk % R]);
+            // dP of the next key tile (dS was read by the dQ MMAs just issued)
+            if (jn < nkt) ok = issue_dp(g + 1);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        first = false;
+        j = jn;
+        ++g;
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&ctl->bar_dq_done);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps 0..7
+    const int qd = warp & 3;
+    const int hf = warp >> 2;
+    const int row = qd * 32 + lane;  // query row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+    bool ok = true;
+    uint32_t g = 0, it = 0;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+      const Item3 w = decode_item(item, nqt, H);
+      const int q = w.t * kBT + row;
+      {
+        // the previous item's MMAs have all completed (its dq_done was waited on)
+        const __nv_bfloat16* src = (hf == 0 ? qg : dog) + (((size_t)w.b * S + q) * H + w.h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (q < S) v = __ldg(reinterpret_cast<const uint4*>(src) + 8 * c + t);
+            wv[4 * t + 0] = v.x;
+            wv[4 * t + 1] = v.y;
+            wv[4 * t + 2] = v.z;
+            wv[4 * t + 3] = v.w;
+          }
+          tmem_st32_bits(tl + (hf == 0 ? kColQ : kColDO) + 32 * c, wv);
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->bar_qdo_ready);
+      }
+      float nl2 = -INFINITY, dl = 0.f;
+      if (q < S) {
+        const float l = lse[((size_t)w.b * H + w.h) * S + q];
+        if (l != -INFINITY) nl2 = -l * kLog2e;
+        dl = delta[((size_t)w.b * H + w.h) * S + q];
+      }
+      int ntiles = 0;
+      for (int j = 0; j < nkt; ++j) {
+        uint32_t words[4];
+        if (kMask) {
+          key_tile_bits(mask, w.b, S, j, words);
+          if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
+        }
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, g & 1, ctx, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        float p[64];
+        tmem_ld32x2(tl + kColS + 64 * hf, tl + kColS + 64 * hf + 32, p);
+        tc_fence_before();
+        mbar_arrive(&ctl->bar_s_read);
+        {
+          const float2 c2 = make_float2(scale_log2, scale_log2);
+          const float2 n2 = make_float2(nl2, nl2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = fma2(make_float2(p[2 * c], p[2 * c + 1]), c2, n2);
+            p[2 * c] = ex2(x.x);
+            p[2 * c + 1] = ex2(x.y);
+          }
+          if (kMask) {
+            const uint32_t w0 = words[2 * hf], w1 = words[2 * hf + 1];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              if (!((w0 >> c) & 1u)) p[c] = 0.f;
+              if (!((w1 >> c) & 1u)) p[32 + c] = 0.f;
+            }
+          } else if ((j + 1) * kBT > S) {
+            const int lim = S - j * kBT - 64 * hf;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c >= lim) p[c] = 0.f;
+          }
+        }
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp_full, g & 1, ctx, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        float dp[64];
+        tmem_ld32x2(tl + kColDP + 64 * hf, tl + kColDP + 64 * hf + 32, dp);
+        {
+          const float2 d2 = make_float2(dl, dl);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 d =
+                mul2(make_float2(p[2 * c], p[2 * c + 1]), sub2(make_float2(dp[2 * c], dp[2 * c + 1]), d2));
+            dp[2 * c] = d.x;
+            dp[2 * c + 1] = d.y;
+          }
+        }
+        store_packed64(tl + kColDP + 64 * hf, dp);
+        tc_fence_before();
+        mbar_arrive(&ctl->bar_ds_ready);
+        ++g;
+        ++ntiles;
+      }
+      if (!ok) break;
+      // epilogue: dQ = scale * (dS K)
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dq_done, it & 1, ctx, ctl));
+      if (!ok) break;
+      tc_fence_after();
+      __nv_bfloat16* drow = dq + (((size_t)w.b * S + q) * H + w.h) * D + hf * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        float gg[32];
+        tmem_ld32(tl + kColDQ + hf * (D / 2) + 32 * c, gg);
+        if (ntiles == 0) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) gg[t] = 0.f;
+        }
+        if (q < S) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint4 v;
+            v.x = pack_bf16(gg[8 * t + 0] * scale, gg[8 * t + 1] * scale);
+            v.y = pack_bf16(gg[8 * t + 2] * scale, gg[8 * t + 3] * scale);
+            v.z = pack_bf16(gg[8 * t + 4] * scale, gg[8 * t + 5] * scale);
+            v.w = pack_bf16(gg[8 * t + 6] * scale, gg[8 * t + 7] * scale);
+            *reinterpret_cast<uint4*>(drow + 32 * c + 8 * t) = v;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl->bar_dq_free);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp && lane == 0 && mma_issued) {
+    mma_commit(&ctl->bar_final);
+    settle(&ctl->bar_final, 0, ctx);
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    for (int s = 0; s < R; ++s)
+      if (kv_armed[s]) settle(&ctl->bar_kv_full[s], (kv_armed[s] - 1) & 1, ctx);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
 int grid_cap(size_t work, int per_block) {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const size_t need = (work + per_block - 1) / per_block;
-  const size_t cap = (size_t)sms * 8;
+  const size_t cap = (size_t)sm_count() * 8;
   return (int)(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
 template <int D, bool kMask>
 int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
                const uint8_t* mask, void* dq, void* dk, void* dv, int B, int S, int H, float scale, float* delta,
-               float* acc, cudaStream_t stream, const DevCtx& ctx) {
+               cudaStream_t stream, const DevCtx& ctx) {
   const size_t rows = (size_t)B * S * H;
-  const size_t acc_vec4 = rows * D / 4;
   bwd_preprocess_kernel<D><<<grid_cap(rows * 8, 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
-      reinterpret_cast<float4*>(acc), B, S, H, acc_vec4);
+      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta, B, S, H);
   int st = check_launch("uaa_attn_bwd (preprocess)");
   if (st) return st;
-  CUtensorMap mq, mk, mv, mdo, macc;
+  CUtensorMap mq, mk, mv, mdo;
   if ((st = encode_bshd_map(&mq, q, B, S, H, D, 128))) return st;
   if ((st = encode_bshd_map(&mk, k, B, S, H, D, 128))) return st;
   if ((st = encode_bshd_map(&mv, v, B, S, H, D, 128))) return st;
   if ((st = encode_bshd_map(&mdo, dout, B, S, H, D, 128))) return st;
-  if ((st = encode_bshd_map_f32(&macc, acc, B, S, H, D, 128))) return st;
-  auto kern = attn_bwd_kernel<D, kMask>;
-  const int smem = BwdLayout<D>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-  dim3 grid((S + kBK - 1) / kBK, H, B);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, macc, lse, delta, mask, static_cast<__nv_bfloat16*>(dk),
-                                         static_cast<__nv_bfloat16*>(dv), S, H, scale, scale * kLog2e, ctx);
-  if ((st = check_launch("uaa_attn_bwd (main)"))) return st;
-  const size_t n8 = rows * D / 8;
-  dq_convert_kernel<<<grid_cap(n8, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
-                                                            static_cast<uint4*>(dq), scale, n8);
-  return check_launch("uaa_attn_bwd (dq convert)");
-}
-
-size_t delta_bytes(int B, int S, int H) {
-  return (((size_t)B * H * S * 4) + 255) & ~(size_t)255;
+  const long long ntiles = (S + kBT - 1) / kBT;
+  const long long items = ntiles * H * B;
+  if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_bwd: too many work items");
+  const int grid = (int)(items < sm_count() ? items : sm_count());
+  {
+    auto kern = attn_bwd_dkdv_kernel<D, kMask>;
+    const int smem = DkdvLayout<D>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, lse, delta, mask, static_cast<__nv_bfloat16*>(dk),
+                                           static_cast<__nv_bfloat16*>(dv), S, H, (int)items, scale,
+                                           scale * kLog2e, ctx);
+    if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
+  }
+  {
+    auto kern = attn_bwd_dq_kernel<D, kMask>;
+    const int smem = DqLayout<D>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, lse, delta, mask, static_cast<const __nv_bfloat16*>(q),
+                                           static_cast<const __nv_bfloat16*>(dout), static_cast<__nv_bfloat16*>(dq),
+                                           S, H, (int)items, scale, scale * kLog2e, ctx);
+    if ((st = check_launch("uaa_attn_bwd (dQ)"))) return st;
+  }
+  return UAA_OK;
 }
 
 }  // namespace
@@ -672,7 +978,7 @@ using namespace uaa;
 
 extern "C" size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D) {
   if (B < 0 || S < 0 || H < 0 || (D != 64 && D != 128)) return 0;
-  return delta_bytes(B, S, H) + (size_t)B * S * H * D * 4;
+  return (((size_t)B * H * S * 4) + 255) & ~(size_t)255;
 }
 
 extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -697,17 +1003,16 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
   DevCtx ctx;
   if ((st = get_dev_ctx(&ctx))) return st;
   float* delta = static_cast<float*>(workspace);
-  float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + delta_bytes(B, S, H));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64)
-    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, acc,
-                                           s, ctx)
-                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta,
-                                            acc, s, ctx);
-  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, acc,
-                                          s, ctx)
-                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, acc,
-                                           s, ctx);
+    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
+                                           ctx)
+                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
+                                            ctx);
+  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
+                                          ctx)
+                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
+                                           ctx);
 }
 
 // ---------------------------------------------------------------------------
@@ -728,8 +1033,8 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
 // caches it; make that first call before any stream capture begins.  All calls
 // share the one array: two calls whose kernels overlap on the GPU (different
 // streams, no ordering between them) race on it and give wrong results.
-// Nothing in the array needs to start at zero: the Delta part is fully written
-// and the dQ accumulator is zeroed by the preprocess kernel of every call.
+// Nothing in the array needs to start at zero: every call rewrites the Delta
+// vector it holds before reading it.
 namespace uaa {
 namespace {
 

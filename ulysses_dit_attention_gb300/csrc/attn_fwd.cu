@@ -8,20 +8,29 @@
 // Ulysses Anything backward", Unsupported cases: the key-padding mask is
 // head-broadcast (B, 1, 1, S).
 //
-// Design (one CTA = one 128-row query tile of one (batch, head)):
-//   warp 4     TMA producer: Q once, then K/V tiles of 128 keys into a
-//              2-stage ring (128-byte swizzled, 64 columns per box); with a
-//              mask it also packs the tile's 128 mask bits into shared memory.
-//   warp 5     tcgen05 issuer (one thread): S_j = Q K_j^T into one of two
-//              TMEM S buffers (S_{j+1} is issued before P_j is ready, so the
-//              tensor core overlaps the softmax), then O += P_j V_j into a
-//              TMEM O accumulator; completion is signalled with tcgen05.commit.
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r), so the row
-//              max and row sum are thread-local; online softmax in base 2,
-//              P_j written as bf16 to shared memory (K-major, swizzled) as the
-//              A operand of the PV MMA; O rescaled in TMEM when the running
-//              max moves; epilogue O / l -> bf16, LSE = m*scale + ln l.
-// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256,256+D) O.
+// Design: a persistent grid (one CTA per SM) walks work items; an item is a
+// pair of 128-row query tiles (256 rows) of one (batch, head).
+//   warp 8     TMA producer: the item's two Q tiles, then K_j, V_j tiles of
+//              128 keys through a 4-stage ring (128-byte swizzled, 64 columns
+//              per box); with a mask it also packs each tile's 128 mask bits
+//              into shared memory.
+//   warp 9     tcgen05 issuer (one thread), ping-pong over the two tiles:
+//                S0_0 S1_0 | PV0_0 S0_1 | PV1_0 S1_1 | PV0_1 S0_2 | ...
+//              so while one softmax warpgroup works on its tile the tensor
+//              core runs the other tile's MMAs.  PV reads P from TMEM (A
+//              operand in tensor memory) and V from shared memory.
+//   warps 0-3  softmax of query tile 0, warps 4-7 softmax of tile 1: thread r
+//              owns query row r (TMEM lane r), so the row max and row sum are
+//              thread-local; online softmax in base 2 with a lazily updated
+//              offset (O is rescaled in TMEM only when the row max grew by
+//              more than 2^8); P is packed to bf16 pairs and stored over the
+//              first 64 columns of the tile's S buffer with tcgen05.st; the
+//              epilogue writes O / l in bf16 and LSE = offset*ln2 + ln l.
+// The S_t of the next key tile is issued after PV_t of the current one: the
+// MMAs of one thread execute in issue order, so PV_t has read P_t before S_t
+// overwrites those columns.
+// TMEM columns: [0,128) S/P of tile 0, [128,256) S/P of tile 1, [256,256+D)
+// O of tile 0, [256+D,256+2D) O of tile 1.
 #include <math.h>
 
 #include "uaa_common.cuh"
@@ -29,40 +38,40 @@
 namespace uaa {
 namespace {
 
-constexpr int kBM = 128;  // query rows per CTA (TMEM lanes)
+constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
 constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes (one swizzle column block)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 template <int D>
 struct FwdLayout {
+  static constexpr int kRing = 4;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + kKStages * kTileBytes;
-  static constexpr int kP = kV + kVStages * kTileBytes;
-  static constexpr int kCtl = kP + kBM * kBN * 2;
-  static constexpr int kBytes = kCtl + 256;
-  // keep one CTA per SM (the 512 TMEM columns are allocated whole)
-  static constexpr int kSmem = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
+  static constexpr int kQ = 0;                                  // two Q tiles
+  static constexpr int kRingOff = kQ + 2 * kTileBytes;          // K/V ring
+  static constexpr int kCtl = kRingOff + kRing * kTileBytes;
+  static constexpr int kSmem = kCtl + 512;
+  static_assert(kSmem <= 232448, "forward shared memory exceeds the per-CTA limit");
 };
 
 struct FwdCtl {
-  uint64_t bar_q;
-  uint64_t bar_k_full[kKStages];
-  uint64_t bar_k_empty[kKStages];
-  uint64_t bar_v_full[kVStages];
-  uint64_t bar_v_empty[kVStages];
+  uint64_t bar_q_full;
+  uint64_t bar_q_empty;
+  uint64_t bar_kv_full[4];
+  uint64_t bar_kv_empty[4];
   uint64_t bar_s_full[2];
-  uint64_t bar_p_full;
-  uint64_t bar_o_full;
+  uint64_t bar_p_full[2];
+  uint64_t bar_pv_done[2];
+  uint64_t bar_o_free;
   uint64_t bar_final;
   uint32_t tmem_base;
   int abort;
-  uint32_t mask_words[kVStages][4];
+  uint32_t mask_words[4][4];  // per ring slot (filled with the V tile)
 };
+static_assert(sizeof(FwdCtl) <= 512, "control block");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -101,54 +110,69 @@ __device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity, const Dev
   if (!mbar_wait(bar, parity, ctx.timeout_ns)) atomicOr(ctx.status, kStatusTimeout);
 }
 
+struct Item {
+  int qp, h, b;
+};
+
+__device__ __forceinline__ Item decode_item(int item, int nqp, int H) {
+  Item it;
+  it.qp = item % nqp;
+  const int bh = item / nqp;
+  it.h = bh % H;
+  it.b = bh / H;
+  return it;
+}
+
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const uint8_t* __restrict__ key_mask,
-                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int S, int H, float scale,
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int S, int H, int num_items,
                     float scale_log2, DevCtx ctx) {
   using L = FwdLayout<D>;
   constexpr int kChunks = D / 64;
+  constexpr int R = L::kRing;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, kBN, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+  constexpr float kLn2 = 0.6931471805599453f;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   FwdCtl* ctl = reinterpret_cast<FwdCtl*>(smem + L::kCtl);
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    // the swizzled operand tiles need 1024-byte alignment; never expected to trigger
+    if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadLaunch);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int q0 = qt * kBM;
+  const int nqp = (S + 2 * kBM - 1) / (2 * kBM);
   const int nkt = (S + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
-    mbar_init(&ctl->bar_q, 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&ctl->bar_k_full[s], 1);
-      mbar_init(&ctl->bar_k_empty[s], 1);
+    mbar_init(&ctl->bar_q_full, 1);
+    mbar_init(&ctl->bar_q_empty, 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(&ctl->bar_kv_full[s], 1);
+      mbar_init(&ctl->bar_kv_empty[s], 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&ctl->bar_v_full[s], 1);
-      mbar_init(&ctl->bar_v_empty[s], 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&ctl->bar_s_full[w], 1);
+      mbar_init(&ctl->bar_p_full[w], 128);
+      mbar_init(&ctl->bar_pv_done[w], 1);
     }
-    mbar_init(&ctl->bar_s_full[0], 1);
-    mbar_init(&ctl->bar_s_full[1], 1);
-    mbar_init(&ctl->bar_p_full, 4 * 32);
-    mbar_init(&ctl->bar_o_full, 1);
+    mbar_init(&ctl->bar_o_free, 256);
     mbar_init(&ctl->bar_final, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, 512);
     tmem_relinquish();
   }
@@ -157,200 +181,240 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  // Teardown bookkeeping of the producer: uses armed per stage.
-  uint32_t k_armed[kKStages] = {0, 0};
-  uint32_t v_armed[kVStages] = {0, 0};
-  bool q_armed = false;
+  // Teardown bookkeeping of the producer: uses armed per barrier.
+  uint32_t kv_armed[4] = {0, 0, 0, 0};
+  uint32_t q_armed = 0;
   bool mma_issued = false;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&ctl->bar_q, L::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) tma_load_4d(smem + L::kQ + c * kChunkBytes, &tmQ, &ctl->bar_q, c * 64, h, q0, b);
-      q_armed = true;
-    }
-    for (int j = 0; j < nkt; ++j) {
-      const int ks = j % kKStages;
-      const uint32_t ku = j / kKStages;
+    uint32_t n = 0;  // K/V ring counter across items
+    uint32_t it = 0;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+      const Item w = decode_item(item, nqp, H);
       if (lane == 0) {
-        if (ku > 0) ok = wait_or_abort(&ctl->bar_k_empty[ks], (ku - 1) & 1, ctx, ctl);
+        if (it > 0) ok = wait_or_abort(&ctl->bar_q_empty, (it - 1) & 1, ctx, ctl);
         if (ok) {
-          mbar_arrive_expect_tx(&ctl->bar_k_full[ks], L::kTileBytes);
+          mbar_arrive_expect_tx(&ctl->bar_q_full, 2 * L::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(smem + L::kK + ks * L::kTileBytes + c * kChunkBytes, &tmK, &ctl->bar_k_full[ks], c * 64, h,
-                        j * kBN, b);
-          k_armed[ks] = ku + 1;
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(smem + L::kQ + t * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full, c * 64, w.h,
+                          w.qp * 2 * kBM + t * kBM, w.b);
+          q_armed = it + 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const int vs = j % kVStages;
-      const uint32_t vu = j / kVStages;
-      if (lane == 0 && vu > 0) ok = wait_or_abort(&ctl->bar_v_empty[vs], (vu - 1) & 1, ctx, ctl);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (kMask) {
-        // bit c of word t = key j*128 + 32t + c is attended
-        uint32_t words[4];
+      for (int j = 0; ok && j < nkt; ++j) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int key = j * kBN + 32 * t + lane;
-          const bool valid = key < S && key_mask[(size_t)b * S + key] != 0;
-          words[t] = __ballot_sync(0xffffffffu, valid);
+        for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
+          const int slot = n % R;
+          const uint32_t use = n / R;
+          if (lane == 0 && use > 0) ok = wait_or_abort(&ctl->bar_kv_empty[slot], (use - 1) & 1, ctx, ctl);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (kMask && kind == 1) {
+            // bit c of word t = key j*128 + 32t + c is attended
+            uint32_t words[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int key = j * kBN + 32 * t + lane;
+              const bool valid = key < S && key_mask[(size_t)w.b * S + key] != 0;
+              words[t] = __ballot_sync(0xffffffffu, valid);
+            }
+            if (lane == 0) {
+#pragma unroll
+              for (int t = 0; t < 4; ++t) ctl->mask_words[slot][t] = words[t];
+            }
+            __syncwarp();
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
+            const CUtensorMap* map = kind == 0 ? &tmK : &tmV;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + c * kChunkBytes, map,
+                          &ctl->bar_kv_full[slot], c * 64, w.h, j * kBN, w.b);
+            kv_armed[slot] = use + 1;
+          }
         }
-        if (lane == 0) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) ctl->mask_words[vs][t] = words[t];
-        }
-        __syncwarp();
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&ctl->bar_v_full[vs], L::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(smem + L::kV + vs * L::kTileBytes + c * kChunkBytes, &tmV, &ctl->bar_v_full[vs], c * 64, h,
-                      j * kBN, b);
-        v_armed[vs] = vu + 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = wait_or_abort(&ctl->bar_q, 0, ctx, ctl);
-      tc_fence_after();
-      const uint32_t sQ = sbase + L::kQ;
-      const uint32_t sP = sbase + L::kP;
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % kKStages;
-        const uint32_t ku = j / kKStages;
-        if (!wait_or_abort(&ctl->bar_k_full[ks], ku & 1, ctx, ctl)) return false;
-        tc_fence_after();
-        const uint32_t sK = sbase + L::kK + ks * L::kTileBytes;
-        const uint32_t d = tmem + (uint32_t)((j & 1) * kBN);
+      bool ok = true;
+      uint32_t g = 0;  // global tile counter across items (phase index of s/p/pv barriers)
+      uint32_t it = 0;
+      auto ring_addr = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
+      auto issue_s = [&](int t, uint32_t nk, uint32_t gg) {
+        const uint32_t sQ = sbase + L::kQ + t * L::kTileBytes;
+        const uint32_t sK = ring_addr(nk);
+        const uint32_t d = tmem + (uint32_t)(t * kBN);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
           mma_bf16(d, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0);
         }
-        mma_commit(&ctl->bar_k_empty[ks]);
-        mma_commit(&ctl->bar_s_full[j & 1]);
-        mma_issued = true;
-        return true;
+        mma_commit(&ctl->bar_s_full[t]);
+        (void)gg;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < nkt; ++j) {
-        if (j + 1 < nkt && !(ok = issue_s(j + 1))) break;
-        if (!(ok = wait_or_abort(&ctl->bar_p_full, j & 1, ctx, ctl))) break;
-        tc_fence_after();
-        const int vs = j % kVStages;
-        if (!(ok = wait_or_abort(&ctl->bar_v_full[vs], (j / kVStages) & 1, ctx, ctl))) break;
-        tc_fence_after();
-        const uint32_t sV = sbase + L::kV + vs * L::kTileBytes;
+      auto issue_pv = [&](int t, uint32_t nv, bool acc) {
+        const uint32_t aP = tmem + (uint32_t)(t * kBN);  // P_t: 128 rows x 128 keys bf16 = 64 columns
+        const uint32_t sV = ring_addr(nv);
+        const uint32_t d = tmem + 256 + (uint32_t)(t * D);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(tmem + 256, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(sV + kk * 2048, kChunkBytes, 1024),
-                   kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(d, aP + kk * 8, sdesc_sw128(sV + kk * 2048, kChunkBytes, 1024), kIdescPV,
+                      (acc || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl->bar_pv_done[t]);
+      };
+      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+        if (!(ok = wait_or_abort(&ctl->bar_q_full, it & 1, ctx, ctl))) break;
+        tc_fence_after();
+        // K_0 of this item: ring index 2g
+        uint32_t nk = 2 * g;
+        if (!(ok = wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl))) break;
+        tc_fence_after();
+        issue_s(0, nk, g);
+        issue_s(1, nk, g);
+        mma_commit(&ctl->bar_kv_empty[nk % R]);
+        mma_issued = true;
+        for (int j = 0; j < nkt; ++j) {
+          const uint32_t gj = g + j;
+          const uint32_t nv = 2 * gj + 1;
+          // tile 0: PV0_j, then S0_{j+1}
+          if (!(ok = wait_or_abort(&ctl->bar_p_full[0], gj & 1, ctx, ctl))) break;
+          tc_fence_after();
+          if (!(ok = wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl))) break;
+          tc_fence_after();
+          if (j == 0 && it > 0) {
+            // the previous item's epilogue must have read O before it is overwritten
+            if (!(ok = wait_or_abort(&ctl->bar_o_free, (it - 1) & 1, ctx, ctl))) break;
+            tc_fence_after();
+          }
+          issue_pv(0, nv, j > 0);
+          const bool more = j + 1 < nkt;
+          const uint32_t nk1 = 2 * (gj + 1);
+          if (more) {
+            if (!(ok = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl))) break;
+            tc_fence_after();
+            issue_s(0, nk1, gj + 1);
+          }
+          // tile 1: PV1_j, then S1_{j+1}
+          if (!(ok = wait_or_abort(&ctl->bar_p_full[1], gj & 1, ctx, ctl))) break;
+          tc_fence_after();
+          issue_pv(1, nv, j > 0);
+          mma_commit(&ctl->bar_kv_empty[nv % R]);
+          if (more) {
+            issue_s(1, nk1, gj + 1);
+            mma_commit(&ctl->bar_kv_empty[nk1 % R]);
+          }
         }
-        mma_commit(&ctl->bar_v_empty[vs]);
-        mma_commit(&ctl->bar_o_full);
+        if (!ok) break;
+        mma_commit(&ctl->bar_q_empty);  // both Q tiles are free once this item's MMAs are done
+        g += nkt;
       }
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warps 0..3
-    const int row = warp * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    uint8_t* sP = smem + L::kP;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row within the tile
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t colS = (uint32_t)(t * kBN);
+    const uint32_t colO = 256 + (uint32_t)(t * D);
     bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full[sb], (j >> 1) & 1, ctx, ctl));
-      if (!ok) break;
-      tc_fence_after();
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld32(tl + sb * kBN + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
-      if (kMask) {
-        const int vs = j % kVStages;
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_v_full[vs], (j / kVStages) & 1, ctx, ctl));
-        if (!ok) break;
-        uint32_t w[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) w[t] = ctl->mask_words[vs][t];
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (!((w[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
-      } else if ((j + 1) * kBN > S) {
-        const int lim = S - j * kBN;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= lim) s[c] = -INFINITY;
-      }
-      float mt = s[0];
-#pragma unroll
-      for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, s[c]);
-      const float m_new = fmaxf(m_run, mt);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new * scale_log2;
-      const float alpha = ex2(m_run * scale_log2 - m_use);
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] = ex2(fmaf(s[c], scale_log2, -m_use));
-        rs += s[c];
-      }
-      l_run = l_run * alpha + rs;
-      m_run = m_new;
-      if (j > 0) {
-        // PV_{j-1} must be done before P is overwritten and O is rescaled
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_o_full, (j - 1) & 1, ctx, ctl));
+    uint32_t g = 0;
+    uint32_t it = 0;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+      const Item w = decode_item(item, nqp, H);
+      float mu = -INFINITY;  // log2-domain offset in use (scaled max, possibly stale by < 2^8)
+      float l_run = 0.f;
+      for (int j = 0; j < nkt; ++j) {
+        const uint32_t gj = g + j;
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full[t], gj & 1, ctx, ctl));
         if (!ok) break;
         tc_fence_after();
-      }
+        float s[kBN];
+        tmem_ld32x2(tl + colS, tl + colS + 32, *reinterpret_cast<float(*)[64]>(&s[0]));
+        tmem_ld32x2(tl + colS + 64, tl + colS + 96, *reinterpret_cast<float(*)[64]>(&s[64]));
+        if (kMask) {
+          const uint32_t nv = 2 * gj + 1;
+          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl));
+          if (!ok) break;
+          uint32_t mw[4];
 #pragma unroll
-      for (int ch = 0; ch < kBN / 64; ++ch) {
+          for (int q = 0; q < 4; ++q) mw[q] = ctl->mask_words[nv % R][q];
 #pragma unroll
-        for (int pc = 0; pc < 8; ++pc) {
-          const float* src = &s[ch * 64 + pc * 8];
-          uint4 v;
-          v.x = pack_bf16(src[0], src[1]);
-          v.y = pack_bf16(src[2], src[3]);
-          v.z = pack_bf16(src[4], src[5]);
-          v.w = pack_bf16(src[6], src[7]);
-          *reinterpret_cast<uint4*>(sP + ch * kChunkBytes + row * 128 + ((pc ^ (row & 7)) << 4)) = v;
+          for (int c = 0; c < kBN; ++c)
+            if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+        } else if ((j + 1) * kBN > S) {
+          const int lim = S - j * kBN;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= lim) s[c] = -INFINITY;
         }
-      }
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        float mt = max3(s[0], s[1], s[2]);
+#pragma unroll
+        for (int c = 3; c + 1 < kBN; c += 2) mt = max3(mt, s[c], s[c + 1]);
+        mt = fmaxf(mt, s[kBN - 1]);
+        const float mt2 = mt * scale_log2;  // -inf if every key of the tile is masked
+        float alpha = 1.f;
+        if (mt2 > mu + kRescaleThreshold) {
+          alpha = ex2(mu - mt2);  // 0 when mu = -inf
+          mu = mt2;
+        }
+        const float mu_use = (mu == -INFINITY) ? 0.f : mu;
+        if (j > 0) {
+          // PV_{j-1} of this tile must be done before its P columns are overwritten and O is rescaled
+          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (gj - 1) & 1, ctx, ctl));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const float2 c2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-mu_use, -mu_use);
+        float2 rs2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = fma2(make_float2(s[64 * hh + 2 * c], s[64 * hh + 2 * c + 1]), c2, nm2);
+            const float2 e = make_float2(ex2(x.x), ex2(x.y));
+            rs2 = add2(rs2, e);
+            pk[c] = pack_bf16(e.x, e.y);
+          }
+          // P (bf16 pairs) over the first 64 columns of this tile's S buffer
+          tmem_st32_bits(tl + colS + 32 * hh, pk);
+        }
+        l_run = l_run * alpha + (rs2.x + rs2.y);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(tl + 256 + 32 * c, o);
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tl + colO + 32 * c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tl + 256 + 32 * c, o);
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tl + colO + 32 * c, o);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(&ctl->bar_p_full[t]);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ctl->bar_p_full);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_o_full, (nkt - 1) & 1, ctx, ctl));
-    if (ok) {
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (g + nkt - 1) & 1, ctx, ctl));
+      if (!ok) break;
       tc_fence_after();
-      const int q = q0 + row;
+      const int q = w.qp * 2 * kBM + t * kBM + row;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = out + (((size_t)b * S + q) * H + h) * D;
+      __nv_bfloat16* orow = out + (((size_t)w.b * S + q) * H + w.h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
-        tmem_ld32(tl + 256 + 32 * c, o);
+        tmem_ld32(tl + colO + 32 * c, o);
         if (q < S) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -363,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (q < S) lse[((size_t)b * H + h) * S + q] = l_run > 0.f ? m_run * scale + logf(l_run) : -INFINITY;
+      tc_fence_before();
+      mbar_arrive(&ctl->bar_o_free);
+      if (q < S) lse[((size_t)w.b * H + w.h) * S + q] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
+      g += nkt;
     }
   }
 
@@ -372,25 +439,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stay bounded.
   tc_fence_before();
   __syncthreads();
-  if (warp == 5 && lane == 0 && mma_issued) {
+  if (warp == kMmaWarp && lane == 0 && mma_issued) {
     // every MMA has completed before TMEM is released
     mma_commit(&ctl->bar_final);
     settle(&ctl->bar_final, 0, ctx);
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     // no TMA write may still be in flight into this CTA's shared memory
-    if (q_armed) settle(&ctl->bar_q, 0, ctx);
-    for (int s = 0; s < kKStages; ++s)
-      if (k_armed[s]) settle(&ctl->bar_k_full[s], (k_armed[s] - 1) & 1, ctx);
-    for (int s = 0; s < kVStages; ++s)
-      if (v_armed[s]) settle(&ctl->bar_v_full[s], (v_armed[s] - 1) & 1, ctx);
+    if (q_armed) settle(&ctl->bar_q_full, (q_armed - 1) & 1, ctx);
+    for (int s = 0; s < R; ++s)
+      if (kv_armed[s]) settle(&ctl->bar_kv_full[s], (kv_armed[s] - 1) & 1, ctx);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess || n <= 0)
+    return 148;
+  return n;
 }
 
 template <int D, bool kMask>
@@ -405,8 +478,11 @@ int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask,
   const int smem = FwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_fwd: smem attribute: %s", cudaGetErrorString(e));
-  dim3 grid((S + kBM - 1) / kBM, H, B);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mask, static_cast<__nv_bfloat16*>(out), lse, S, H, scale,
+  const long long nqp = (S + 2 * kBM - 1) / (2 * kBM);
+  const long long items = nqp * H * B;
+  if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_fwd: too many work items");
+  const int grid = (int)(items < sm_count() ? items : sm_count());
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mask, static_cast<__nv_bfloat16*>(out), lse, S, H, (int)items,
                                          scale * kLog2e, ctx);
   return check_launch("uaa_attn_fwd");
 }
