@@ -37,7 +37,19 @@ if ROOT not in sys.path:
 from ulysses_dit_attention_gb300 import synth  # noqa: E402
 
 WORKLOAD = "ulysses_p4_n27280_h40_d128"
+
+# DRAM bytes per attn_bwd_dkdv_kernel launch (one 10-head group of the workload above), from the
+# ncu capture summarised in profiles/, keyed by the SHA-256 prefix of the attn_bwd.cu it was taken
+# on; the bench reports null once the kernel source has changed since.
+DKDV_TRAFFIC = {}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def dkdv_traffic():
+    import hashlib
+    src = os.path.join(ROOT, "ulysses_dit_attention_gb300", "csrc", "attn_bwd.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return DKDV_TRAFFIC.get(h)
 
 
 def flops(B, S, H, D, fwd=True, bwd=True):
@@ -236,6 +248,12 @@ def run_gpu(args, world, rank, local):
     ws = torch.empty(uaa.attn_bwd_workspace_bytes(B, S, Hg, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = {}
+    # per-call events around the backward's dK/dV and dQ kernels (created and recorded once up front)
+    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps * P)]
+    for trio in prof:
+        for e in trio:
+            e.record(stream)
+    prof_iter = iter(prof)
 
     def mark(name):
         e = torch.cuda.Event(enable_timing=True)
@@ -264,9 +282,11 @@ def run_gpu(args, world, rank, local):
         for g in range(P):
             if timed:
                 mark("bwd0")
+                uaa.set_bwd_profile_events(next(prof_iter))
             uaa.attn_bwd(yq[g], yk[g], yv[g], yo[g], ydo[g], lse[g], None, w.scale, dq=ydq[g], dk=ydk[g],
                          dv=ydv[g], workspace=ws)
             if timed:
+                uaa.set_bwd_profile_events(None)
                 mark("bwd1")
         if timed:
             mark("h2s_g0")
@@ -342,11 +362,15 @@ def run_gpu(args, world, rank, local):
     pk, src = peaks()
     peak_tf, key = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops")
     peak_hbm, _ = _peak_value(pk, "hbm_gbs")
-    bwd_flops_launch = flops(B, S, Hg, D, fwd=False)
-    achieved = bwd_flops_launch / (bwd_launch * 1e-3) / 1e12
+    dkdv_ms = sum(a.elapsed_time(b) for a, b, _ in prof) / len(prof)
+    dq_ms = sum(b.elapsed_time(c) for _, b, c in prof) / len(prof)
+    # dK/dV kernel: the S, dP, dV and dK GEMMs of one head group = 8*B*Hg*S^2*D algorithmic FLOPs
+    dkdv_flops = 8 * B * Hg * S * S * D
+    achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "traffic": None,
-                "kernel": "uaa_attn_bwd (Delta preprocess + K/V-tile-major backward + dQ convert), one head group",
+                "frac": achieved / peak_tf, "traffic": dkdv_traffic(),
+                "kernel": "attn_bwd_dkdv_kernel<128,false> (one head group: S, dP, dV, dK GEMMs)",
+                "flops_per_launch": dkdv_flops, "ms_per_launch": dkdv_ms,
                 "peak_source": f"{src} {key}"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -363,6 +387,9 @@ def run_gpu(args, world, rank, local):
         "attn_fwd_tflops": flops(B, S, H, D, bwd=False) / (fwd_ms * 1e-3) / 1e12,
         "attn_bwd_tflops": flops(B, S, H, D, fwd=False) / (bwd_ms * 1e-3) / 1e12,
         "fwd_launch_tflops": flops(B, S, Hg, D, bwd=False) / (fwd_launch * 1e-3) / 1e12,
+        "kernel_ms_per_launch": {"attn_fwd_kernel": fwd_launch, "attn_bwd_dkdv_kernel": dkdv_ms,
+                                 "attn_bwd_dq_kernel": dq_ms},
+        "dq_kernel_tflops": (6 * B * Hg * S * S * D) / (dq_ms * 1e-3) / 1e12,
         "relayout_gbs": relayout_bytes / (relayout_ms * 1e-3) / 1e9,
         "relayout_hbm_frac": (relayout_bytes / (relayout_ms * 1e-3) / 1e9) / peak_hbm if peak_hbm else None,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

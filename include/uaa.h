@@ -98,6 +98,14 @@ int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                  void* dq, void* dk, void* dv, int B, int S, int H, int D, float scale,
                  void* workspace, size_t workspace_bytes, uaa_stream_t stream);
 
+/* Profiling aid (off by default; the pages have no counterpart): when the
+ * three CUDA events (cudaEvent_t, created by the caller) are non-NULL, every
+ * later uaa_attn_bwd call of the calling thread records `before_dkdv` just
+ * before its dK/dV kernel, `after_dkdv` between the dK/dV and dQ kernels and
+ * `after_dq` after the dQ kernel, on the call's stream, so each kernel can be
+ * timed on its own.  Pass NULLs to stop.  The events stay owned by the caller. */
+void uaa_set_bwd_profile_events(void* before_dkdv, void* after_dkdv, void* after_dq);
+
 /* Allocation-free variant of uaa_attn_bwd.  The source pages have no
  * counterpart; this entry point exists for callers that cannot allocate device
  * memory when they run the backward -- code running inside an allocator

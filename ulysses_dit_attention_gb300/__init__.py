@@ -25,7 +25,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "seq_to_head", "head_to_seq",
-    "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms", "Attention",
+    "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms",
+    "set_bwd_profile_events", "Attention",
     "attention", "UlyssesAttention", "ulysses_attention", "STATUS",
 ]
 
@@ -57,6 +58,7 @@ _SIGS = {
     "uaa_check_device_status": (_I, [_P]),
     "uaa_watchdog_selftest": (_I, [ctypes.c_uint, _P]),
     "uaa_set_wait_timeout_ms": (None, [ctypes.c_uint]),
+    "uaa_set_bwd_profile_events": (None, [_P, _P, _P]),
     "uaa_last_error": (ctypes.c_char_p, []),
     "uaa_version": (ctypes.c_char_p, []),
 }
@@ -276,6 +278,15 @@ def watchdog_selftest(timeout_us=2000, device=None):
 
 def set_wait_timeout_ms(ms: int):
     lib().uaa_set_wait_timeout_ms(int(ms))
+
+
+def set_bwd_profile_events(events=None):
+    """Record three ``torch.cuda.Event``s around the backward's dK/dV and dQ kernels (None stops)."""
+    if events is None:
+        lib().uaa_set_bwd_profile_events(None, None, None)
+    else:
+        a, b, c = (_P(e.cuda_event) for e in events)
+        lib().uaa_set_bwd_profile_events(a, b, c)
 
 
 # --------------------------------------------------------------------------- Ulysses composition

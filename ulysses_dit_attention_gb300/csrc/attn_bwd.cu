@@ -930,6 +930,16 @@ int grid_cap(size_t work, int per_block) {
   return (int)(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
+// Optional profiling events of the calling thread (uaa_set_bwd_profile_events).
+thread_local cudaEvent_t t_prof_events[3] = {nullptr, nullptr, nullptr};
+
+int record_prof(int i, cudaStream_t stream) {
+  if (!t_prof_events[i]) return UAA_OK;
+  cudaError_t e = cudaEventRecord(t_prof_events[i], stream);
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: profiling event: %s", cudaGetErrorString(e));
+  return UAA_OK;
+}
+
 template <int D, bool kMask>
 int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
                const uint8_t* mask, void* dq, void* dk, void* dv, int B, int S, int H, float scale, float* delta,
@@ -948,6 +958,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
   const long long items = ntiles * H * B;
   if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_bwd: too many work items");
   const int grid = (int)(items < sm_count() ? items : sm_count());
+  if ((st = record_prof(0, stream))) return st;
   {
     auto kern = attn_bwd_dkdv_kernel<D, kMask>;
     const int smem = DkdvLayout<D>::kSmem;
@@ -958,6 +969,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
                                            scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
   }
+  if ((st = record_prof(1, stream))) return st;
   {
     auto kern = attn_bwd_dq_kernel<D, kMask>;
     const int smem = DqLayout<D>::kSmem;
@@ -968,13 +980,19 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
                                            S, H, (int)items, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dQ)"))) return st;
   }
-  return UAA_OK;
+  return record_prof(2, stream);
 }
 
 }  // namespace
 }  // namespace uaa
 
 using namespace uaa;
+
+extern "C" void uaa_set_bwd_profile_events(void* before_dkdv, void* after_dkdv, void* after_dq) {
+  t_prof_events[0] = static_cast<cudaEvent_t>(before_dkdv);
+  t_prof_events[1] = static_cast<cudaEvent_t>(after_dkdv);
+  t_prof_events[2] = static_cast<cudaEvent_t>(after_dq);
+}
 
 extern "C" size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D) {
   if (B < 0 || S < 0 || H < 0 || (D != 64 && D != 128)) return 0;
