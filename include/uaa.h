@@ -75,8 +75,9 @@ int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key
                  void* out, float* lse, int B, int S, int H, int D, float scale,
                  uaa_stream_t stream);
 
-/* Bytes of device workspace uaa_attn_bwd needs for (B, S, H, D): the fp32
- * (B, H, S) row-dot vector Delta = rowsum(dO * O), rounded up to 256 bytes.
+/* Bytes of device workspace uaa_attn_bwd needs for (B, S, H, D): two fp32
+ * (B, H, S_pad) vectors, S_pad = S rounded up to a multiple of 128 -- the row
+ * dot Delta = rowsum(dO * O) and -LSE * log2(e) -- rounded up to 256 bytes.
  * Returns 0 for invalid sizes. */
 size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D);
 

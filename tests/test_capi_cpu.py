@@ -36,7 +36,8 @@ def test_exports_every_declared_symbol(L):
 def test_workspace_bytes(L):
     B, S, H, D = 1, 27280, 40, 128
     got = L.uaa_attn_bwd_workspace_bytes(B, S, H, D)
-    assert got == (B * H * S * 4 + 255) // 256 * 256  # the fp32 Delta vector only
+    s_pad = (S + 127) // 128 * 128
+    assert got == (B * H * s_pad * 8 + 255) // 256 * 256  # fp32 Delta and -LSE*log2e, rows padded to 128
     assert L.uaa_attn_bwd_workspace_bytes(1, 16, 2, 96) == 0
 
 

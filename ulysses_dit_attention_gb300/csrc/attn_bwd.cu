@@ -11,7 +11,10 @@
 // Three kernels, no atomics and no reductions, so every gradient is
 // deterministic:
 //  1. bwd_preprocess_kernel: Delta_i = sum_d dO_id * O_id (fp32), which equals
-//     sum_j P_ij dP_ij.
+//     sum_j P_ij dP_ij, and -LSE_i*log2(e), both into the workspace as (B, H,
+//     S_pad) rows padded to a whole number of 128-row tiles (padding: Delta = 0,
+//     -LSE*log2e = -inf, so padded rows get P = 0), which the dK/dV producer
+//     copies into shared memory with one bulk copy per tile.
 //  2. attn_bwd_dkdv_kernel (K/V-tile-major): a persistent CTA takes a 128-key
 //     tile of one (batch, head) and loops over all 128-row query tiles:
 //        S^T  = K Q^T,  P^T = exp2(S^T*c - lse2)            (M = keys)
@@ -141,7 +144,9 @@ __device__ __forceinline__ uint32_t packed_a_col(int kk) { return kk < 4 ? kk * 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
-                                                             float* __restrict__ delta, int B, int S, int H) {
+                                                             const float* __restrict__ lse,
+                                                             float* __restrict__ delta, float* __restrict__ nl2,
+                                                             int B, int S, int S_pad, int H) {
   constexpr int kVecPerRow = D / 8;
   constexpr int kPerLane = kVecPerRow / 8;
   const size_t rows = (size_t)B * S * H;
@@ -176,10 +181,22 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       const size_t bs = r / H;
       const int s = (int)(bs % S);
       const int b = (int)(bs / S);
-      delta[((size_t)b * H + h) * S + s] = acc;
+      const float l = lse[((size_t)b * H + h) * S + s];
+      delta[((size_t)b * H + h) * S_pad + s] = acc;
+      nl2[((size_t)b * H + h) * S_pad + s] = l == -INFINITY ? -INFINITY : -l * kLog2e;
     }
   }
+  // padding rows [S, S_pad) of every (b, h)
+  const int padn = S_pad - S;
+  for (size_t i = tid; i < (size_t)B * H * padn; i += nthreads) {
+    const size_t bh = i / padn;
+    const int s = S + (int)(i % padn);
+    delta[bh * S_pad + s] = 0.f;
+    nl2[bh * S_pad + s] = -INFINITY;
+  }
 }
+
+__host__ __device__ constexpr int padded_rows(int S) { return (S + 127) / 128 * 128; }
 
 // ---------------------------------------------------------------------------
 // 2. dK / dV (K/V-tile-major)
@@ -214,7 +231,7 @@ template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                         const float* __restrict__ lse, const float* __restrict__ delta,
+                         const float* __restrict__ nl2, const float* __restrict__ delta,
                          const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ dk,
                          __nv_bfloat16* __restrict__ dv, int S, int H, int num_items, float scale,
                          float scale_log2, DevCtx ctx) {
@@ -299,52 +316,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const float* lse_bh = lse + ((size_t)w.b * H + w.h) * S;
-      const float* delta_bh = delta + ((size_t)w.b * H + w.h) * S;
+      const size_t row0 = ((size_t)w.b * H + w.h) * padded_rows(S);
       for (int i = 0; ok && i < nqt; ++i, ++nq) {
         const int qs = nq % L::kQStages;
         const uint32_t qu = nq / L::kQStages;
         const int ds = nq % L::kDStages;
         const uint32_t du = nq / L::kDStages;
-        if (lane == 0 && qu > 0) ok = wait_or_abort(&ctl->bar_q_empty[qs], (qu - 1) & 1, ctx, ctl);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int q = i * kBT + 32 * t + lane;
-          sDelta[qs * kBT + 32 * t + lane] = q < S ? delta_bh[q] : 0.f;
-        }
-        __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->bar_q_full[qs], L::kTileBytes);
+          // Q_i with its Delta row, then dO_i with its -LSE*log2e row (rows past S
+          // were written as Delta = 0 and -inf by the preprocess kernel)
+          if (qu > 0) ok = wait_or_abort(&ctl->bar_q_empty[qs], (qu - 1) & 1, ctx, ctl);
+          if (ok) {
+            mbar_arrive_expect_tx(&ctl->bar_q_full[qs], L::kTileBytes + kBT * 4);
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(smem + L::kQ + qs * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full[qs], c * 64,
-                        w.h, i * kBT, w.b);
-          q_armed[qs] = qu + 1;
-          if (du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int q = i * kBT + 32 * t + lane;
-          float nl2 = -INFINITY;  // -LSE*log2(e): rows past the end and fully masked rows get P = 0
-          if (q < S) {
-            const float l = lse_bh[q];
-            if (l != -INFINITY) nl2 = -l * kLog2e;
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(smem + L::kQ + qs * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full[qs], c * 64,
+                          w.h, i * kBT, w.b);
+            bulk_load(sDelta + qs * kBT, delta + row0 + (size_t)i * kBT, kBT * 4, &ctl->bar_q_full[qs]);
+            q_armed[qs] = qu + 1;
+            if (du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
           }
-          sLse[ds * kBT + 32 * t + lane] = nl2;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes);
+          if (ok) {
+            mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes + kBT * 4);
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(smem + L::kDO + ds * L::kTileBytes + c * kChunkBytes, &tmDO, &ctl->bar_do_full[ds], c * 64,
-                        w.h, i * kBT, w.b);
-          do_armed[ds] = du + 1;
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(smem + L::kDO + ds * L::kTileBytes + c * kChunkBytes, &tmDO, &ctl->bar_do_full[ds], c * 64,
+                          w.h, i * kBT, w.b);
+            bulk_load(sLse + ds * kBT, nl2 + row0 + (size_t)i * kBT, kBT * 4, &ctl->bar_do_full[ds]);
+            do_armed[ds] = du + 1;
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       ++it;
     }
@@ -363,11 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_s = [&](uint32_t g) -> bool {
           if (!wait_or_abort(&ctl->bar_q_full[g % L::kQStages], (g / L::kQStages) & 1, ctx, ctl)) return false;
           tc_fence_after();
+          const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dq0 = sdesc_sw128(sq(g), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_bf16(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sq(g) + off, 16, 1024), kIdescKK,
-                     kk > 0);
+            mma_bf16(tmem + kColS, desc_add(dk0, off), desc_add(dq0, off), kIdescKK, kk > 0);
           }
           mma_commit(&ctl->bar_s_full);
           return true;
@@ -375,11 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_dp = [&](uint32_t g) -> bool {
           if (!wait_or_abort(&ctl->bar_do_full[g % L::kDStages], (g / L::kDStages) & 1, ctx, ctl)) return false;
           tc_fence_after();
+          const uint64_t dv0 = sdesc_sw128(sV, 16, 1024), ddo0 = sdesc_sw128(sdo(g), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_bf16(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdo(g) + off, 16, 1024),
-                     kIdescKK, kk > 0);
+            mma_bf16(tmem + kColDP, desc_add(dv0, off), desc_add(ddo0, off), kIdescKK, kk > 0);
           }
           mma_commit(&ctl->bar_dp_full);
           return true;
@@ -399,20 +401,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_or_abort(&ctl->bar_acc_free, (it - 1) & 1, ctx, ctl))) break;
             tc_fence_after();
           }
+          {
+            const uint64_t b0 = sdesc_sw128(sdo(g), kChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBT / 16; ++kk)
-            mma_bf16_ts(tmem + kColDV, tmem + kColS + packed_a_col(kk),
-                        sdesc_sw128(sdo(g) + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBT / 16; ++kk)
+              mma_bf16_ts(tmem + kColDV, tmem + kColS + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
+                          (i > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(&ctl->bar_do_empty[g % L::kDStages]);
           // S^T of the next tile (P^T was read by the dV MMAs just issued)
           if (i + 1 < nqt && !(ok = issue_s(g + 1))) break;
           // dK += dS^T Q  (A = dS^T in the dP^T columns)
           if (!(ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl))) break;
           tc_fence_after();
+          {
+            const uint64_t b0 = sdesc_sw128(sq(g), kChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBT / 16; ++kk)
-            mma_bf16_ts(tmem + kColDK, tmem + kColDP + packed_a_col(kk),
-                        sdesc_sw128(sq(g) + kk * 2048, kChunkBytes, 1024), kIdescKM, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBT / 16; ++kk)
+              mma_bf16_ts(tmem + kColDK, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
+                          (i > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(&ctl->bar_q_empty[g % L::kQStages]);
           // dP^T of the next tile (dS^T was read by the dK MMAs just issued)
           if (i + 1 < nqt && !(ok = issue_dp(g + 1))) break;
@@ -590,7 +598,7 @@ template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const float* __restrict__ lse, const float* __restrict__ delta,
+                       const float* __restrict__ nl2g, const float* __restrict__ delta,
                        const uint8_t* __restrict__ key_mask, const __nv_bfloat16* __restrict__ qg,
                        const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int S, int H,
                        int num_items, float scale, float scale_log2, DevCtx ctx) {
@@ -705,10 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t nk = 2 * gg;
         if (!wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl)) return false;
         tc_fence_after();
+        const uint64_t b0 = sdesc_sw128(ring(nk), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, sdesc_sw128(ring(nk) + off, 16, 1024), kIdescKK, kk > 0);
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(&ctl->bar_s_full);
         return true;
@@ -717,11 +726,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t nv = 2 * gg + 1;
         if (!wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl)) return false;
         tc_fence_after();
+        const uint64_t b0 = sdesc_sw128(ring(nv), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, sdesc_sw128(ring(nv) + off, 16, 1024), kIdescKK,
-                      kk > 0);
+          mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(&ctl->bar_dp_full);
         mma_commit(&ctl->bar_kv_empty[nv % R]);  // V_j is only read by this dP
@@ -752,10 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             tc_fence_after();
             const uint32_t nk = 2 * g;
+            const uint64_t b0 = sdesc_sw128(ring(nk), kChunkBytes, 1024);
 #pragma unroll
             for (int kk = 0; kk < kBT / 16; ++kk)
-              mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk),
-                          sdesc_sw128(ring(nk) + kk * 2048, kChunkBytes, 1024), kIdescKM,
+              mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
                           (!first || kk > 0) ? 1u : 0u);
             mma_commit(&ctl->bar_kv_empty[nk % R]);
             // dP of the next key tile (dS was read by the dQ MMAs just issued)
@@ -802,12 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&ctl->bar_qdo_ready);
       }
-      float nl2 = -INFINITY, dl = 0.f;
-      if (q < S) {
-        const float l = lse[((size_t)w.b * H + w.h) * S + q];
-        if (l != -INFINITY) nl2 = -l * kLog2e;
-        dl = delta[((size_t)w.b * H + w.h) * S + q];
-      }
+      // rows past S read the padding (-inf, 0)
+      const size_t prow = ((size_t)w.b * H + w.h) * padded_rows(S) + q;
+      const float nl2 = nl2g[prow];
+      const float dl = delta[prow];
       int ntiles = 0;
       for (int j = 0; j < nkt; ++j) {
         uint32_t words[4];
@@ -945,8 +952,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
                const uint8_t* mask, void* dq, void* dk, void* dv, int B, int S, int H, float scale, float* delta,
                cudaStream_t stream, const DevCtx& ctx) {
   const size_t rows = (size_t)B * S * H;
+  float* nl2 = delta + (size_t)B * H * padded_rows(S);
   bwd_preprocess_kernel<D><<<grid_cap(rows * 8, 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta, B, S, H);
+      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, nl2, B, S,
+      padded_rows(S), H);
   int st = check_launch("uaa_attn_bwd (preprocess)");
   if (st) return st;
   CUtensorMap mq, mk, mv, mdo;
@@ -964,7 +973,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, lse, delta, mask, static_cast<__nv_bfloat16*>(dk),
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
                                            static_cast<__nv_bfloat16*>(dv), S, H, (int)items, scale,
                                            scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
@@ -975,7 +984,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DqLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, lse, delta, mask, static_cast<const __nv_bfloat16*>(q),
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<const __nv_bfloat16*>(q),
                                            static_cast<const __nv_bfloat16*>(dout), static_cast<__nv_bfloat16*>(dq),
                                            S, H, (int)items, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dQ)"))) return st;
@@ -996,7 +1005,8 @@ extern "C" void uaa_set_bwd_profile_events(void* before_dkdv, void* after_dkdv, 
 
 extern "C" size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D) {
   if (B < 0 || S < 0 || H < 0 || (D != 64 && D != 128)) return 0;
-  return (((size_t)B * H * S * 4) + 255) & ~(size_t)255;
+  // Delta and -LSE*log2e, each (B, H, S_pad) fp32, S_pad = S rounded up to 128
+  return (((size_t)B * H * padded_rows(S) * 8) + 255) & ~(size_t)255;
 }
 
 extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -1052,7 +1062,7 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
 // share the one array: two calls whose kernels overlap on the GPU (different
 // streams, no ordering between them) race on it and give wrong results.
 // Nothing in the array needs to start at zero: every call rewrites the Delta
-// vector it holds before reading it.
+// and -LSE*log2e vectors it holds (padding rows included) before reading them.
 namespace uaa {
 namespace {
 

@@ -11,7 +11,7 @@
 // Design: a persistent grid (one CTA per SM) walks work items; an item is a
 // pair of 128-row query tiles (256 rows) of one (batch, head).
 //   warp 8     TMA producer: the item's two Q tiles, then K_j, V_j tiles of
-//              128 keys through a 4-stage ring (128-byte swizzled, 64 columns
+//              128 keys through a 5-stage ring (128-byte swizzled, 64 columns
 //              per box); with a mask it also packs each tile's 128 mask bits
 //              into shared memory.
 //   warp 9     tcgen05 issuer (one thread), ping-pong over the two tiles:
@@ -48,20 +48,21 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when th
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kRing = 4;
+  static constexpr int kRing = 5;
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kQ = 0;                                  // two Q tiles
   static constexpr int kRingOff = kQ + 2 * kTileBytes;          // K/V ring
   static constexpr int kCtl = kRingOff + kRing * kTileBytes;
   static constexpr int kSmem = kCtl + 512;
   static_assert(kSmem <= 232448, "forward shared memory exceeds the per-CTA limit");
+  static_assert(kRing <= 5, "control block holds five ring slots");
 };
 
 struct FwdCtl {
   uint64_t bar_q_full;
   uint64_t bar_q_empty;
-  uint64_t bar_kv_full[4];
-  uint64_t bar_kv_empty[4];
+  uint64_t bar_kv_full[5];
+  uint64_t bar_kv_empty[5];
   uint64_t bar_s_full[2];
   uint64_t bar_p_full[2];
   uint64_t bar_pv_done[2];
@@ -69,7 +70,7 @@ struct FwdCtl {
   uint64_t bar_final;
   uint32_t tmem_base;
   int abort;
-  uint32_t mask_words[4][4];  // per ring slot (filled with the V tile)
+  uint32_t mask_words[5][4];  // per ring slot (filled with the V tile)
 };
 static_assert(sizeof(FwdCtl) <= 512, "control block");
 
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
 
   // Teardown bookkeeping of the producer: uses armed per barrier.
-  uint32_t kv_armed[4] = {0, 0, 0, 0};
+  uint32_t kv_armed[5] = {0, 0, 0, 0, 0};
   uint32_t q_armed = 0;
   bool mma_issued = false;
 
@@ -253,10 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sQ = sbase + L::kQ + t * L::kTileBytes;
         const uint32_t sK = ring_addr(nk);
         const uint32_t d = tmem + (uint32_t)(t * kBN);
+        const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dk0 = sdesc_sw128(sK, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(d, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0);
+          mma_bf16(d, desc_add(dq0, off), desc_add(dk0, off), kIdescS, kk > 0);
         }
         mma_commit(&ctl->bar_s_full[t]);
         (void)gg;
@@ -265,9 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aP = tmem + (uint32_t)(t * kBN);  // P_t: 128 rows x 128 keys bf16 = 64 columns
         const uint32_t sV = ring_addr(nv);
         const uint32_t d = tmem + 256 + (uint32_t)(t * D);
+        const uint64_t dv0 = sdesc_sw128(sV, kChunkBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(d, aP + kk * 8, sdesc_sw128(sV + kk * 2048, kChunkBytes, 1024), kIdescPV,
+          mma_bf16_ts(d, aP + kk * 8, desc_add(dv0, kk * 2048), kIdescPV,
                       (acc || kk > 0) ? 1u : 0u);
         mma_commit(&ctl->bar_pv_done[t]);
       };

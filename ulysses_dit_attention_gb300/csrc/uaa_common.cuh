@@ -119,6 +119,14 @@ __device__ __forceinline__ void tma_reduce_add_4d(const void* smem_src, const CU
       "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// 1-D bulk copy of `bytes` from global to shared memory completing on `bar`
+// (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk group of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
@@ -333,6 +341,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Descriptor of the same operand advanced by `byte_off` bytes.  Shared-memory
+// addresses stay below 256 KB, so the 14-bit start-address field never carries
+// into the neighbouring fields and one 32-bit add on the low word suffices; the
+// MMA issuer adds a constant per K step instead of re-encoding the descriptor.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (byte_off >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
 }
 
 #endif  // __CUDACC__
