@@ -3,10 +3,13 @@
 One step = one pass of the whole path over the Ulysses emulation workload
 (B=1, N=27280 split into P=4 virtual sequence shards of 6821/6821/6819/6819
 rows, H=40, D=128, bf16 N(0,1) inputs):
-  seq->head exchange of Q, K, V -> attention forward per 10-head group (O, LSE)
-  -> head->seq exchange of O -> seq->head exchange of dO -> attention backward
-  per group (Delta preprocess, K/V-tile-major backward, dQ convert)
-  -> head->seq exchange of dQ, dK, dV.
+  seq->head exchange of Q, K, V -> attention forward of the four 10-head
+  groups (O, LSE) -> head->seq exchange of O -> seq->head exchange of dO ->
+  attention backward of the groups (Delta preprocess, K/V-tile-major dK/dV
+  kernel, Q-tile-major dQ kernel) -> head->seq exchange of dQ, dK, dV.
+The four head groups are contiguous (P, B, N, H/P, D) tensors, i.e. one BSHD
+tensor of batch P*B, so each attention kernel runs once over all groups (the
+work one GPU does for the four emulated ranks, in one launch).
 Every step runs through the C ABI (``libuaa.so``).
 
 ``value`` = attention fwd+bwd FLOPs (4*B*H*S^2*D + 10*B*H*S^2*D) per second of
@@ -245,11 +248,11 @@ def run_gpu(args, world, rank, local):
     yo, ydq, ydk, ydv = (torch.empty_like(yq) for _ in range(4))
     lse = torch.empty((P, B, Hg, S), dtype=torch.float32, device=dev)
     o_sh, dq_sh, dk_sh, dv_sh = (torch.empty_like(sh["q"]) for _ in range(4))
-    ws = torch.empty(uaa.attn_bwd_workspace_bytes(B, S, Hg, D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(uaa.attn_bwd_workspace_bytes(P * B, S, Hg, D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = {}
     # per-call events around the backward's dK/dV and dQ kernels (created and recorded once up front)
-    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps * P)]
+    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for trio in prof:
         for e in trio:
             e.record(stream)
@@ -267,27 +270,28 @@ def run_gpu(args, world, rank, local):
             uaa.seq_to_head(sh[n], lens, out=y)
         if timed:
             mark("s2h_fwd1")
-        for g in range(P):
-            if timed:
-                mark("fwd0")
-            uaa.attn_fwd(yq[g], yk[g], yv[g], None, w.scale, out=yo[g], lse=lse[g])
-            if timed:
-                mark("fwd1")
+        if timed:
+            mark("fwd0")
+        # all P head groups in one launch: (P, B, N, Hg, D) is a BSHD tensor of batch P*B
+        uaa.attn_fwd(yq.view(P * B, S, Hg, D), yk.view(P * B, S, Hg, D), yv.view(P * B, S, Hg, D), None, w.scale,
+                     out=yo.view(P * B, S, Hg, D), lse=lse.view(P * B, Hg, S))
+        if timed:
+            mark("fwd1")
         if timed:
             mark("h2s_o0")
         uaa.head_to_seq(yo, lens, cap, out=o_sh)
         uaa.seq_to_head(sh["do"], lens, out=ydo)
         if timed:
             mark("h2s_o1")
-        for g in range(P):
-            if timed:
-                mark("bwd0")
-                uaa.set_bwd_profile_events(next(prof_iter))
-            uaa.attn_bwd(yq[g], yk[g], yv[g], yo[g], ydo[g], lse[g], None, w.scale, dq=ydq[g], dk=ydk[g],
-                         dv=ydv[g], workspace=ws)
-            if timed:
-                uaa.set_bwd_profile_events(None)
-                mark("bwd1")
+        if timed:
+            mark("bwd0")
+            uaa.set_bwd_profile_events(next(prof_iter))
+        g4 = lambda t: t.view(P * B, S, Hg, D)  # noqa: E731
+        uaa.attn_bwd(g4(yq), g4(yk), g4(yv), g4(yo), g4(ydo), lse.view(P * B, Hg, S), None, w.scale, dq=g4(ydq),
+                     dk=g4(ydk), dv=g4(ydv), workspace=ws)
+        if timed:
+            uaa.set_bwd_profile_events(None)
+            mark("bwd1")
         if timed:
             mark("h2s_g0")
         for y, x in ((ydq, dq_sh), (ydk, dk_sh), (ydv, dv_sh)):
@@ -295,7 +299,7 @@ def run_gpu(args, world, rank, local):
         if timed:
             mark("h2s_g1")
 
-    launches_per_step = 3 + P + 1 + 1 + 3 * P + 3
+    launches_per_step = 3 + 1 + 1 + 1 + 3 + 3
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -364,12 +368,12 @@ def run_gpu(args, world, rank, local):
     peak_hbm, _ = _peak_value(pk, "hbm_gbs")
     dkdv_ms = sum(a.elapsed_time(b) for a, b, _ in prof) / len(prof)
     dq_ms = sum(b.elapsed_time(c) for _, b, c in prof) / len(prof)
-    # dK/dV kernel: the S, dP, dV and dK GEMMs of one head group = 8*B*Hg*S^2*D algorithmic FLOPs
-    dkdv_flops = 8 * B * Hg * S * S * D
+    # dK/dV kernel: the S, dP, dV and dK GEMMs of all P head groups = 8*P*B*Hg*S^2*D algorithmic FLOPs
+    dkdv_flops = 8 * P * B * Hg * S * S * D
     achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": dkdv_traffic(),
-                "kernel": "attn_bwd_dkdv_kernel<128,false> (one head group: S, dP, dV, dK GEMMs)",
+                "kernel": "attn_bwd_dkdv_kernel<128,false> (all head groups: S, dP, dV, dK GEMMs)",
                 "flops_per_launch": dkdv_flops, "ms_per_launch": dkdv_ms,
                 "peak_source": f"{src} {key}"}
     cpu = None
@@ -386,10 +390,10 @@ def run_gpu(args, world, rank, local):
         "parts_ms_per_step": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms, "relayout": relayout_ms},
         "attn_fwd_tflops": flops(B, S, H, D, bwd=False) / (fwd_ms * 1e-3) / 1e12,
         "attn_bwd_tflops": flops(B, S, H, D, fwd=False) / (bwd_ms * 1e-3) / 1e12,
-        "fwd_launch_tflops": flops(B, S, Hg, D, bwd=False) / (fwd_launch * 1e-3) / 1e12,
+        "fwd_launch_tflops": flops(P * B, S, Hg, D, bwd=False) / (fwd_launch * 1e-3) / 1e12,
         "kernel_ms_per_launch": {"attn_fwd_kernel": fwd_launch, "attn_bwd_dkdv_kernel": dkdv_ms,
                                  "attn_bwd_dq_kernel": dq_ms},
-        "dq_kernel_tflops": (6 * B * Hg * S * S * D) / (dq_ms * 1e-3) / 1e12,
+        "dq_kernel_tflops": (6 * P * B * Hg * S * S * D) / (dq_ms * 1e-3) / 1e12,
         "relayout_gbs": relayout_bytes / (relayout_ms * 1e-3) / 1e9,
         "relayout_hbm_frac": (relayout_bytes / (relayout_ms * 1e-3) / 1e9) / peak_hbm if peak_hbm else None,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

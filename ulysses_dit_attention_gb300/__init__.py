@@ -290,6 +290,11 @@ def set_bwd_profile_events(events=None):
 
 
 # --------------------------------------------------------------------------- Ulysses composition
+def _flat(t):
+    """(P, B, N, Hg, D) head groups as one BSHD tensor of batch P*B (a view, no copy)."""
+    return t.flatten(0, 1)
+
+
 class UlyssesAttention(torch.autograd.Function):
     """Ulysses attention over P emulated ranks on one device.
 
@@ -307,8 +312,12 @@ class UlyssesAttention(torch.autograd.Function):
         P = yq.shape[0]
         o = torch.empty_like(yq)
         lse = torch.empty((P, yq.shape[1], yq.shape[3], yq.shape[2]), dtype=torch.float32, device=yq.device)
-        for g in range(P):
-            attn_fwd(yq[g], yk[g], yv[g], key_mask, scale, out=o[g], lse=lse[g])
+        if key_mask is None:
+            # the P groups form one BSHD tensor of batch P*B: one launch for all emulated ranks
+            attn_fwd(_flat(yq), _flat(yk), _flat(yv), None, scale, out=_flat(o), lse=lse.flatten(0, 1))
+        else:
+            for g in range(P):
+                attn_fwd(yq[g], yk[g], yv[g], key_mask, scale, out=o[g], lse=lse[g])
         o_sh = head_to_seq(o, shard_lens, cap)
         ctx.save_for_backward(yq, yk, yv, o, lse)
         ctx.shard_lens, ctx.key_mask, ctx.scale, ctx.cap = tuple(shard_lens), key_mask, scale, cap
@@ -321,11 +330,14 @@ class UlyssesAttention(torch.autograd.Function):
         ydo = seq_to_head(do_sh.contiguous(), ctx.shard_lens)
         P = yq.shape[0]
         dq, dk, dv = torch.empty_like(yq), torch.empty_like(yq), torch.empty_like(yq)
-        g0 = yq[0]
-        ws = torch.empty(attn_bwd_workspace_bytes(*g0.shape), dtype=torch.uint8, device=yq.device)
-        for g in range(P):
-            attn_bwd(yq[g], yk[g], yv[g], o[g], ydo[g], lse[g], ctx.key_mask, ctx.scale, dq=dq[g], dk=dk[g],
-                     dv=dv[g], workspace=ws)
+        if ctx.key_mask is None:
+            attn_bwd(_flat(yq), _flat(yk), _flat(yv), _flat(o), _flat(ydo), lse.flatten(0, 1), None, ctx.scale,
+                     dq=_flat(dq), dk=_flat(dk), dv=_flat(dv))
+        else:
+            ws = torch.empty(attn_bwd_workspace_bytes(*yq[0].shape), dtype=torch.uint8, device=yq.device)
+            for g in range(P):
+                attn_bwd(yq[g], yk[g], yv[g], o[g], ydo[g], lse[g], ctx.key_mask, ctx.scale, dq=dq[g], dk=dk[g],
+                         dv=dv[g], workspace=ws)
         return (head_to_seq(dq, ctx.shard_lens, ctx.cap), head_to_seq(dk, ctx.shard_lens, ctx.cap),
                 head_to_seq(dv, ctx.shard_lens, ctx.cap), None, None, None)
 

@@ -360,10 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kBN; ++c)
             if (c >= lim) s[c] = -INFINITY;
         }
-        float mt = max3(s[0], s[1], s[2]);
+        // row max over the tile: eight independent chains (the max sits on the
+        // critical path between S_t and PV_t), then a short tree
+        float m8[8];
 #pragma unroll
-        for (int c = 3; c + 1 < kBN; c += 2) mt = max3(mt, s[c], s[c + 1]);
-        mt = fmaxf(mt, s[kBN - 1]);
+        for (int q = 0; q < 8; ++q) m8[q] = fmaxf(s[q], s[q + 8]);
+#pragma unroll
+        for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) m8[q] = max3(m8[q], s[c + q], s[c + q + 8]);
+        const float mt = fmaxf(max3(m8[0], m8[1], m8[2]), max3(max3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
         const float mt2 = mt * scale_log2;  // -inf if every key of the tile is masked
         float alpha = 1.f;
         if (mt2 > mu + kRescaleThreshold) {
