@@ -462,16 +462,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t g = nq + i;
         const int qs = g % L::kQStages;
         const int ds = g % L::kDStages;
+        // -LSE*log2e of Q_i sits with the dO_i stage, Delta_i with the Q_i stage;
+        // both have landed before S^T_i completes, so these waits stay off the
+        // path from S^T_i to P^T_i
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_do_full[ds], (g / L::kDStages) & 1, ctx, ctl));
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[qs], (g / L::kQStages) & 1, ctx, ctl));
+        if (!ok) break;
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, g & 1, ctx, ctl));
         if (!ok) break;
         tc_fence_after();
         float p[64];
         tmem_ld32x2(tl + kColS + 64 * hf, tl + kColS + 64 * hf + 32, p);
-        // -LSE*log2e of Q_i sits with the dO_i stage, Delta_i with the Q_i stage
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_do_full[ds], (g / L::kDStages) & 1, ctx, ctl));
-        if (!ok) break;
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[qs], (g / L::kQStages) & 1, ctx, ctl));
-        if (!ok) break;
         {
           const float2* nl2 = reinterpret_cast<const float2*>(sLse + ds * kBT + 64 * hf);
           const float2 c2 = make_float2(scale_log2, scale_log2);

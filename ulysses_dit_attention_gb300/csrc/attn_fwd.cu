@@ -377,12 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mu = mt2;
         }
         const float mu_use = (mu == -INFINITY) ? 0.f : mu;
-        if (j > 0) {
-          // PV_{j-1} of this tile must be done before its P columns are overwritten and O is rescaled
-          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (gj - 1) & 1, ctx, ctl));
-          if (!ok) break;
-          tc_fence_after();
-        }
+        // PV_{j-1} of this tile, which reads the P columns about to be overwritten
+        // and accumulates the O about to be rescaled, has completed: it was
+        // issued before S_j, and the commit behind s_full covers every earlier
+        // MMA of the issuing thread.
         const float2 c2 = make_float2(scale_log2, scale_log2);
         const float2 nm2 = make_float2(-mu_use, -mu_use);
         float2 rs2 = make_float2(0.f, 0.f);
