@@ -362,8 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
         auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
-        auto issue_s = [&](uint32_t g) -> bool {
-          if (!wait_or_abort(&ctl->bar_q_full[g % L::kQStages], (g / L::kQStages) & 1, ctx, ctl)) return false;
+        // Inside the query loop the compute warps arrive on p_ready / ds_ready
+        // only after they have seen Q_{i+1} / dO_{i+1} land, so the S^T / dP^T
+        // MMAs of the next tile need no wait of their own there: each wait of
+        // the issuing thread costs the tensor pipe a few hundred cycles (it
+        // queues only about one MMA).
+        auto issue_s = [&](uint32_t g, bool wait) -> bool {
+          if (wait && !wait_or_abort(&ctl->bar_q_full[g % L::kQStages], (g / L::kQStages) & 1, ctx, ctl))
+            return false;
           tc_fence_after();
           const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dq0 = sdesc_sw128(sq(g), 16, 1024);
 #pragma unroll
@@ -374,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&ctl->bar_s_full);
           return true;
         };
-        auto issue_dp = [&](uint32_t g) -> bool {
-          if (!wait_or_abort(&ctl->bar_do_full[g % L::kDStages], (g / L::kDStages) & 1, ctx, ctl)) return false;
+        auto issue_dp = [&](uint32_t g, bool wait) -> bool {
+          if (wait && !wait_or_abort(&ctl->bar_do_full[g % L::kDStages], (g / L::kDStages) & 1, ctx, ctl))
+            return false;
           tc_fence_after();
           const uint64_t dv0 = sdesc_sw128(sV, 16, 1024), ddo0 = sdesc_sw128(sdo(g), 16, 1024);
 #pragma unroll
@@ -388,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         ok = wait_or_abort(&ctl->bar_kv_full, it & 1, ctx, ctl);
         tc_fence_after();
-        if (ok) ok = issue_s(nq);
-        if (ok) ok = issue_dp(nq);
+        if (ok) ok = issue_s(nq, true);
+        if (ok) ok = issue_dp(nq, true);
         mma_issued = true;
         for (int i = 0; ok && i < nqt; ++i) {
           const uint32_t g = nq + i;
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&ctl->bar_do_empty[g % L::kDStages]);
           // S^T of the next tile (P^T was read by the dV MMAs just issued)
-          if (i + 1 < nqt && !(ok = issue_s(g + 1))) break;
+          if (i + 1 < nqt && !(ok = issue_s(g + 1, false))) break;
           // dK += dS^T Q  (A = dS^T in the dP^T columns)
           if (!(ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl))) break;
           tc_fence_after();
@@ -423,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&ctl->bar_q_empty[g % L::kQStages]);
           // dP^T of the next tile (dS^T was read by the dK MMAs just issued)
-          if (i + 1 < nqt && !(ok = issue_dp(g + 1))) break;
+          if (i + 1 < nqt && !(ok = issue_dp(g + 1, false))) break;
         }
         if (ok) {
           mma_commit(&ctl->bar_acc_done);
@@ -469,6 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[qs], (g / L::kQStages) & 1, ctx, ctl));
         if (!ok) break;
+        if (i + 1 < nqt) {
+          // Q_{i+1}, read by the S^T MMA that this tile's p_ready releases
+          const uint32_t g1 = g + 1;
+          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_q_full[g1 % L::kQStages], (g1 / L::kQStages) & 1,
+                                                     ctx, ctl));
+          if (!ok) break;
+        }
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, g & 1, ctx, ctl));
         if (!ok) break;
         tc_fence_after();
@@ -492,6 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_packed64(tl + kColS + 64 * hf, p);
         tc_fence_before();
         mbar_arrive(&ctl->bar_p_ready);
+        if (i + 1 < nqt) {
+          // dO_{i+1}, read by the dP^T MMA that this tile's ds_ready releases
+          const uint32_t g1 = g + 1;
+          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_do_full[g1 % L::kDStages], (g1 / L::kDStages) & 1,
+                                                     ctx, ctl));
+          if (!ok) break;
+        }
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp_full, g & 1, ctx, ctl));
         if (!ok) break;
         tc_fence_after();

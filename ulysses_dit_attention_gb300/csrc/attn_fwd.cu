@@ -288,10 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nkt; ++j) {
           const uint32_t gj = g + j;
           const uint32_t nv = 2 * gj + 1;
-          // tile 0: PV0_j, then S0_{j+1}
+          // tile 0: PV0_j, then S0_{j+1}.  The softmax warpgroups arrive on
+          // p_full only after they have seen V_j and K_{j+1} land, so this thread
+          // waits on nothing else inside the loop: each wait of the issuing
+          // thread costs the tensor pipe a few hundred cycles (it queues only
+          // about one MMA).
           if (!(ok = wait_or_abort(&ctl->bar_p_full[0], gj & 1, ctx, ctl))) break;
-          tc_fence_after();
-          if (!(ok = wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl))) break;
           tc_fence_after();
           if (j == 0 && it > 0) {
             // the previous item's epilogue must have read O before it is overwritten
@@ -301,11 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(0, nv, j > 0);
           const bool more = j + 1 < nkt;
           const uint32_t nk1 = 2 * (gj + 1);
-          if (more) {
-            if (!(ok = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl))) break;
-            tc_fence_after();
-            issue_s(0, nk1, gj + 1);
-          }
+          if (more) issue_s(0, nk1, gj + 1);
           // tile 1: PV1_j, then S1_{j+1}
           if (!(ok = wait_or_abort(&ctl->bar_p_full[1], gj & 1, ctx, ctl))) break;
           tc_fence_after();
@@ -338,6 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l_run = 0.f;
       for (int j = 0; j < nkt; ++j) {
         const uint32_t gj = g + j;
+        {
+          // V_j and K_{j+1}, read by the MMAs that this step's p_full releases,
+          // have normally landed long before S_j completes: waiting here keeps
+          // these waits off both the issuing thread and the S -> P path
+          const uint32_t nv = 2 * gj + 1, nk1 = nv + 1;
+          bool okw = wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl);
+          if (okw && j + 1 < nkt) okw = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl);
+          ok = __all_sync(0xffffffffu, okw);
+          if (!ok) break;
+        }
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full[t], gj & 1, ctx, ctl));
         if (!ok) break;
         tc_fence_after();
@@ -345,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32x2(tl + colS, tl + colS + 32, *reinterpret_cast<float(*)[64]>(&s[0]));
         tmem_ld32x2(tl + colS + 64, tl + colS + 96, *reinterpret_cast<float(*)[64]>(&s[64]));
         if (kMask) {
+          // the producer wrote V_j's mask words before arming kv_full, which this
+          // warp has already waited on
           const uint32_t nv = 2 * gj + 1;
-          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl));
-          if (!ok) break;
           uint32_t mw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) mw[q] = ctl->mask_words[nv % R][q];
