@@ -732,9 +732,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       j = next_tile(0);
-      auto issue_s = [&](uint32_t gg) -> bool {
+      // Past the first key tile of an item the compute warps arrive on s_read /
+      // ds_ready only after they have seen K / V of the next tile land, so these
+      // MMAs need no wait of their own there: each wait of the issuing thread
+      // costs the tensor pipe a few hundred cycles (it queues only about one MMA).
+      auto issue_s = [&](uint32_t gg, bool wait) -> bool {
         const uint32_t nk = 2 * gg;
-        if (!wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl)) return false;
+        if (wait && !wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl)) return false;
         tc_fence_after();
         const uint64_t b0 = sdesc_sw128(ring(nk), 16, 1024);
 #pragma unroll
@@ -745,9 +749,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&ctl->bar_s_full);
         return true;
       };
-      auto issue_dp = [&](uint32_t gg) -> bool {
+      auto issue_dp = [&](uint32_t gg, bool wait) -> bool {
         const uint32_t nv = 2 * gg + 1;
-        if (!wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl)) return false;
+        if (wait && !wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl)) return false;
         tc_fence_after();
         const uint64_t b0 = sdesc_sw128(ring(nv), 16, 1024);
 #pragma unroll
@@ -761,8 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (j < nkt) {
         if (lane == 0) {
-          ok = issue_s(g);
-          if (ok) ok = issue_dp(g);
+          ok = issue_s(g, true);
+          if (ok) ok = issue_dp(g, true);
           mma_issued = true;
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
             if (ok) {
               tc_fence_after();
-              ok = issue_s(g + 1);
+              ok = issue_s(g + 1, false);
             }
           }
           // dQ += dS K_j  (A = dS in the dP columns)
@@ -791,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (!first || kk > 0) ? 1u : 0u);
             mma_commit(&ctl->bar_kv_empty[nk % R]);
             // dP of the next key tile (dS was read by the dQ MMAs just issued)
-            if (jn < nkt) ok = issue_dp(g + 1);
+            if (jn < nkt) ok = issue_dp(g + 1, false);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -844,6 +848,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kMask) {
           key_tile_bits(mask, w.b, S, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
+        }
+        // is there a next key tile?  Its K and V are read by the MMAs this tile's
+        // s_read and ds_ready release; they normally land long before, and
+        // waiting for them here keeps these waits off the issuing thread.
+        bool has_next = j + 1 < nkt;
+        if (kMask) {
+          int jn = j + 1;
+          while (jn < nkt && !key_tile_any(mask, w.b, S, jn)) ++jn;
+          has_next = jn < nkt;
+        }
+        if (has_next) {
+          const uint32_t nk1 = 2 * (g + 1), nv1 = nk1 + 1;
+          bool okw = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl);
+          if (okw) okw = wait_or_abort(&ctl->bar_kv_full[nv1 % R], (nv1 / R) & 1, ctx, ctl);
+          ok = __all_sync(0xffffffffu, okw);
+          if (!ok) break;
         }
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full, g & 1, ctx, ctl));
         if (!ok) break;
