@@ -41,10 +41,10 @@ from ulysses_dit_attention_gb300 import synth  # noqa: E402
 
 WORKLOAD = "ulysses_p4_n27280_h40_d128"
 
-# DRAM bytes per attn_bwd_dkdv_kernel launch (one 10-head group of the workload above), from the
-# ncu capture summarised in profiles/, keyed by the SHA-256 prefix of the attn_bwd.cu it was taken
-# on; the bench reports null once the kernel source has changed since.
-DKDV_TRAFFIC = {}
+# DRAM bytes (read + write) per attn_bwd_dkdv_kernel launch (all four 10-head groups of the workload
+# above), from the one-pass ncu capture summarised in profiles/, keyed by the SHA-256 prefix of the
+# attn_bwd.cu it was taken on; the bench reports null once the kernel source has changed since.
+DKDV_TRAFFIC = {"588b85e19c93e957": 1133441024 + 533295104}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
