@@ -34,7 +34,7 @@
 //
 // Warp roles in both main kernels: warps 0-7 compute (TMEM lane quadrant =
 // warp % 4, column half = warp / 4), warp 8 TMA producer, warp 9 tcgen05
-// issuer.  An MMA that overwrites TMEM columns an earlier MMA of the same
+// issuer (the dK/dV kernel has a second issuer, warp 10, taking turns with it).  An MMA that overwrites TMEM columns an earlier MMA of the same
 // thread reads is issued after it: the MMAs of one thread execute in order.
 #include <math.h>
 
@@ -53,8 +53,10 @@ constexpr int kBT = 128;  // rows per query tile and per key tile
 constexpr int kChunkBytes = 128 * 128;
 constexpr int kComputeThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // the dQ kernel's issuer; in the dK/dV kernel the dV / S^T issuer
+constexpr int kMmaWarp1 = 10;  // the dK / dP^T issuer of the dK/dV kernel
 constexpr int kThreads = 320;
+constexpr int kThreadsDkdv = 352;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -221,14 +223,15 @@ struct DkdvCtl {
   uint64_t bar_q_full[3], bar_q_empty[3];
   uint64_t bar_do_full[2], bar_do_empty[2];
   uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready;
-  uint64_t bar_acc_done, bar_acc_free, bar_final;
+  uint64_t bar_acc_done, bar_acc_free, bar_final[2];
   uint32_t tmem_base;
   int abort;
+  uint32_t turn;  // MMA-issue token: bursts released so far
 };
 static_assert(sizeof(DkdvCtl) <= 256, "control block");
 
 template <int D, bool kMask>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsDkdv, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const float* __restrict__ nl2, const float* __restrict__ delta,
@@ -258,24 +261,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
+    // buffers read by both issuers (K/V, Q_i, dO_i) are released by a commit of each
     mbar_init(&ctl->bar_kv_full, 1);
-    mbar_init(&ctl->bar_kv_empty, 1);
+    mbar_init(&ctl->bar_kv_empty, 2);
     for (int s = 0; s < L::kQStages; ++s) {
       mbar_init(&ctl->bar_q_full[s], 1);
-      mbar_init(&ctl->bar_q_empty[s], 1);
+      mbar_init(&ctl->bar_q_empty[s], 2);
     }
     for (int s = 0; s < L::kDStages; ++s) {
       mbar_init(&ctl->bar_do_full[s], 1);
-      mbar_init(&ctl->bar_do_empty[s], 1);
+      mbar_init(&ctl->bar_do_empty[s], 2);
     }
     mbar_init(&ctl->bar_s_full, 1);
     mbar_init(&ctl->bar_dp_full, 1);
     mbar_init(&ctl->bar_p_ready, kComputeThreads);
     mbar_init(&ctl->bar_ds_ready, kComputeThreads);
-    mbar_init(&ctl->bar_acc_done, 1);
+    mbar_init(&ctl->bar_acc_done, 2);
     mbar_init(&ctl->bar_acc_free, kComputeThreads);
-    mbar_init(&ctl->bar_final, 1);
+    mbar_init(&ctl->bar_final[0], 1);
+    mbar_init(&ctl->bar_final[1], 1);
     ctl->abort = 0;
+    ctl->turn = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -350,91 +356,110 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++it;
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer (lane 0 issues)
+  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+    // ------------------------------------------------------------ MMA issuers (lane 0 of warps 9 and 10)
+    // The four GEMMs of a query tile form two chains, each issued by its own
+    // thread:
+    //   warp 9  (chain v): S^T_0 | dV_0 S^T_1 | dV_1 S^T_2 | ...   (after p_ready)
+    //   warp 10 (chain k): dP^T_0 | dK_0 dP^T_1 | dK_1 dP^T_2 | ... (after ds_ready)
+    // The two threads take turns burst by burst (a token in shared memory), so
+    // the tensor pipe runs v, k, v, k, ... and each thread does its barrier
+    // waits while the other's burst runs; the token is handed over four MMAs
+    // before the end of a burst.  The tensor pipe queues only about one MMA,
+    // and a single issuing thread that stopped to wait between GEMMs would leave
+    // it idle for a few hundred cycles per wait.  Within a chain the MMAs of one
+    // thread execute in order: dV_i reads P^T_i before S^T_{i+1} overwrites
+    // those columns, and dK_i reads dS^T_i before dP^T_{i+1} does.
+    const int c = warp - kMmaWarp;  // 0: chain v, 1: chain k
     bool ok = true;
     uint32_t nq = 0, it = 0;
+    uint32_t m = 0;  // bursts of this thread so far; its burst m has turn 2m + c
     const uint32_t sK = sbase + L::kK;
     const uint32_t sV = sbase + L::kV;
+    volatile uint32_t* turn = &ctl->turn;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
       if (kMask && !key_tile_any(mask, w.b, S, w.t)) continue;
       if (lane == 0) {
         auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
         auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
-        // Inside the query loop the compute warps arrive on p_ready / ds_ready
-        // only after they have seen Q_{i+1} / dO_{i+1} land, so the S^T / dP^T
-        // MMAs of the next tile need no wait of their own there: each wait of
-        // the issuing thread costs the tensor pipe a few hundred cycles (it
-        // queues only about one MMA).
-        auto issue_s = [&](uint32_t g, bool wait) -> bool {
-          if (wait && !wait_or_abort(&ctl->bar_q_full[g % L::kQStages], (g / L::kQStages) & 1, ctx, ctl))
-            return false;
-          tc_fence_after();
-          const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dq0 = sdesc_sw128(sq(g), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_bf16(tmem + kColS, desc_add(dk0, off), desc_add(dq0, off), kIdescKK, kk > 0);
+        auto take_turn = [&]() -> bool {
+          const uint32_t want = 2 * m + (uint32_t)c;
+          if (*turn >= want) return true;
+          const uint64_t t0 = globaltimer_ns();
+          while (*turn < want) {
+            if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+            if (globaltimer_ns() - t0 > ctx.timeout_ns) {
+              atomicOr(ctx.status, kStatusTimeout);
+              *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+              return false;
+            }
           }
-          mma_commit(&ctl->bar_s_full);
           return true;
         };
-        auto issue_dp = [&](uint32_t g, bool wait) -> bool {
-          if (wait && !wait_or_abort(&ctl->bar_do_full[g % L::kDStages], (g / L::kDStages) & 1, ctx, ctl))
-            return false;
-          tc_fence_after();
-          const uint64_t dv0 = sdesc_sw128(sV, 16, 1024), ddo0 = sdesc_sw128(sdo(g), 16, 1024);
+        auto pass_turn = [&]() { *turn = 2 * m + (uint32_t)c + 1; };
+        // the first GEMM of a chain for query tile g: S^T_g = K Q_g^T or dP^T_g = V dO_g^T;
+        // hands the token over when `pass` after its first D/16 - 4 MMAs
+        auto issue_first = [&](uint32_t g, bool pass) {
+          const uint64_t a0 = sdesc_sw128(c == 0 ? sK : sV, 16, 1024);
+          const uint64_t b0 = sdesc_sw128(c == 0 ? sq(g) : sdo(g), 16, 1024);
+          const uint32_t d = tmem + (c == 0 ? kColS : kColDP);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_bf16(tmem + kColDP, desc_add(dv0, off), desc_add(ddo0, off), kIdescKK, kk > 0);
+            mma_bf16(d, desc_add(a0, off), desc_add(b0, off), kIdescKK, kk > 0);
+            if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
           }
-          mma_commit(&ctl->bar_dp_full);
-          return true;
+          mma_commit(c == 0 ? &ctl->bar_s_full : &ctl->bar_dp_full);
+          // this thread's read of Q_g (chain v) / dO_g (chain k)
+          mma_commit(c == 0 ? &ctl->bar_q_empty[g % L::kQStages] : &ctl->bar_do_empty[g % L::kDStages]);
+        };
+        // the accumulating GEMM of tile g: dV += P^T dO_g (A = P^T in the S^T columns) or
+        // dK += dS^T Q_g (A = dS^T in the dP^T columns)
+        auto issue_acc = [&](uint32_t g, bool first_acc, bool pass) {
+          const uint64_t b0 = sdesc_sw128(c == 0 ? sdo(g) : sq(g), kChunkBytes, 1024);
+          const uint32_t d = tmem + (c == 0 ? kColDV : kColDK);
+          const uint32_t a = tmem + (c == 0 ? kColS : kColDP);
+#pragma unroll
+          for (int kk = 0; kk < kBT / 16; ++kk) {
+            mma_bf16_ts(d, a + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM, (!first_acc || kk > 0) ? 1u : 0u);
+            if (pass && kk == kBT / 16 - 5) pass_turn();
+          }
+          mma_commit(c == 0 ? &ctl->bar_do_empty[g % L::kDStages] : &ctl->bar_q_empty[g % L::kQStages]);
         };
         ok = wait_or_abort(&ctl->bar_kv_full, it & 1, ctx, ctl);
-        tc_fence_after();
-        if (ok) ok = issue_s(nq, true);
-        if (ok) ok = issue_dp(nq, true);
-        mma_issued = true;
+        if (ok) {
+          ok = c == 0 ? wait_or_abort(&ctl->bar_q_full[nq % L::kQStages], (nq / L::kQStages) & 1, ctx, ctl)
+                      : wait_or_abort(&ctl->bar_do_full[nq % L::kDStages], (nq / L::kDStages) & 1, ctx, ctl);
+        }
+        if (ok) ok = take_turn();
+        if (ok) {
+          tc_fence_after();
+          issue_first(nq, true);
+          ++m;
+          mma_issued = true;
+        }
+        // Inside the query loop the compute warps arrive on p_ready / ds_ready only
+        // after they have seen Q_{i+1} / dO_{i+1} land, so no other wait is needed.
         for (int i = 0; ok && i < nqt; ++i) {
           const uint32_t g = nq + i;
-          // dV += P^T dO  (A = P^T in the S^T columns)
-          if (!(ok = wait_or_abort(&ctl->bar_p_ready, g & 1, ctx, ctl))) break;
-          tc_fence_after();
+          if (!(ok = wait_or_abort(c == 0 ? &ctl->bar_p_ready : &ctl->bar_ds_ready, g & 1, ctx, ctl))) break;
           if (i == 0 && it > 0) {
             // the previous item's epilogue must have read dK / dV
             if (!(ok = wait_or_abort(&ctl->bar_acc_free, (it - 1) & 1, ctx, ctl))) break;
-            tc_fence_after();
           }
-          {
-            const uint64_t b0 = sdesc_sw128(sdo(g), kChunkBytes, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kBT / 16; ++kk)
-              mma_bf16_ts(tmem + kColDV, tmem + kColS + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
-                          (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&ctl->bar_do_empty[g % L::kDStages]);
-          // S^T of the next tile (P^T was read by the dV MMAs just issued)
-          if (i + 1 < nqt && !(ok = issue_s(g + 1, false))) break;
-          // dK += dS^T Q  (A = dS^T in the dP^T columns)
-          if (!(ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl))) break;
+          if (!(ok = take_turn())) break;
           tc_fence_after();
-          {
-            const uint64_t b0 = sdesc_sw128(sq(g), kChunkBytes, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kBT / 16; ++kk)
-              mma_bf16_ts(tmem + kColDK, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
-                          (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&ctl->bar_q_empty[g % L::kQStages]);
-          // dP^T of the next tile (dS^T was read by the dK MMAs just issued)
-          if (i + 1 < nqt && !(ok = issue_dp(g + 1, false))) break;
+          const bool more = i + 1 < nqt;
+          issue_acc(g, i == 0, !more);
+          if (more) issue_first(g + 1, true);
+          ++m;
         }
         if (ok) {
           mma_commit(&ctl->bar_acc_done);
           mma_commit(&ctl->bar_kv_empty);
+        } else {
+          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer may be waiting for our turn
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -576,9 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp && lane == 0 && mma_issued) {
-    mma_commit(&ctl->bar_final);
-    settle(&ctl->bar_final, 0, ctx);
+  if ((warp == kMmaWarp || warp == kMmaWarp1) && lane == 0 && mma_issued) {
+    mma_commit(&ctl->bar_final[warp - kMmaWarp]);
+    settle(&ctl->bar_final[warp - kMmaWarp], 0, ctx);
   }
   if (warp == kProducerWarp && lane == 0) {
     if (kv_armed) settle(&ctl->bar_kv_full, (kv_armed - 1) & 1, ctx);
@@ -1016,7 +1041,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
+    kern<<<grid, kThreadsDkdv, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
                                            static_cast<__nv_bfloat16*>(dv), S, H, (int)items, scale,
                                            scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
