@@ -34,7 +34,7 @@
 //
 // Warp roles in both main kernels: warps 0-7 compute (TMEM lane quadrant =
 // warp % 4, column half = warp / 4), warp 8 TMA producer, warp 9 tcgen05
-// issuer (the dK/dV kernel has a second issuer, warp 10, taking turns with it).  An MMA that overwrites TMEM columns an earlier MMA of the same
+// issuer and warp 10 a second issuer, the two taking turns burst by burst.  An MMA that overwrites TMEM columns an earlier MMA of the same
 // thread reads is issued after it: the MMAs of one thread execute in order.
 #include <math.h>
 
@@ -53,10 +53,9 @@ constexpr int kBT = 128;  // rows per query tile and per key tile
 constexpr int kChunkBytes = 128 * 128;
 constexpr int kComputeThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;    // the dQ kernel's issuer; in the dK/dV kernel the dV / S^T issuer
-constexpr int kMmaWarp1 = 10;  // the dK / dP^T issuer of the dK/dV kernel
-constexpr int kThreads = 320;
-constexpr int kThreadsDkdv = 352;
+constexpr int kMmaWarp = 9;    // first MMA issuer (dK/dV kernel: dV / S^T chain; dQ kernel: S chain)
+constexpr int kMmaWarp1 = 10;  // second MMA issuer (dK/dV kernel: dK / dP^T chain; dQ kernel: dQ / dP chain)
+constexpr int kThreads = 352;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -231,7 +230,7 @@ struct DkdvCtl {
 static_assert(sizeof(DkdvCtl) <= 256, "control block");
 
 template <int D, bool kMask>
-__global__ void __launch_bounds__(kThreadsDkdv, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const float* __restrict__ nl2, const float* __restrict__ delta,
@@ -636,9 +635,10 @@ struct DqCtl {
   uint64_t bar_qdo_ready;
   uint64_t bar_kv_full[8], bar_kv_empty[8];
   uint64_t bar_s_full, bar_s_read, bar_dp_full, bar_ds_ready;
-  uint64_t bar_dq_done, bar_dq_free, bar_final;
+  uint64_t bar_dq_done, bar_dq_free, bar_final[2];
   uint32_t tmem_base;
   int abort;
+  uint32_t turn;  // MMA-issue token: bursts released so far
 };
 static_assert(sizeof(DqCtl) <= 512, "control block");
 
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->bar_qdo_ready, kComputeThreads);
     for (int s = 0; s < R; ++s) {
       mbar_init(&ctl->bar_kv_full[s], 1);
-      mbar_init(&ctl->bar_kv_empty[s], 1);
+      mbar_init(&ctl->bar_kv_empty[s], 2);  // one release per issuer
     }
     mbar_init(&ctl->bar_s_full, 1);
     mbar_init(&ctl->bar_s_read, kComputeThreads);
@@ -683,8 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->bar_ds_ready, kComputeThreads);
     mbar_init(&ctl->bar_dq_done, 1);
     mbar_init(&ctl->bar_dq_free, kComputeThreads);
-    mbar_init(&ctl->bar_final, 1);
+    mbar_init(&ctl->bar_final[0], 1);
+    mbar_init(&ctl->bar_final[1], 1);
     ctl->abort = 0;
+    ctl->turn = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -736,92 +738,137 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer (lane 0 issues)
+  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+    // ------------------------------------------------------------ MMA issuers (lane 0 of warps 9 and 10)
+    // Two chains, each issued by its own thread, per processed key tile g:
+    //   warp 9  (chain s): S_0 | S_1 | S_2 | ...            (S_{g+1} after s_read(g))
+    //   warp 10 (chain d): dP_0 | dQ_0 dP_1 | dQ_1 dP_2 | ... (after ds_ready(g))
+    // The threads take turns burst by burst (a token in shared memory; chain s
+    // passes an empty burst after the last tile so both have the same count),
+    // so each waits for its handshake while the other's burst runs; the token
+    // is handed over four MMAs before the end of a burst.  The tensor pipe
+    // queues only about one MMA, and a single issuing thread that stopped to
+    // wait between GEMMs would leave it idle for a few hundred cycles per wait.
+    // In chain d, dQ_g reads dS_g (in the dP columns) before dP_{g+1}
+    // overwrites them: the MMAs of one thread execute in order.
+    const int c = warp - kMmaWarp;  // 0: chain s, 1: chain d
     bool ok = true;
     uint32_t g = 0, it = 0;  // g: processed key tiles across items
+    uint32_t m = 0;          // bursts of this thread so far; its burst m has turn 2m + c
+    volatile uint32_t* turn = &ctl->turn;
     auto ring = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
+    auto take_turn = [&]() -> bool {
+      const uint32_t want = 2 * m + (uint32_t)c;
+      if (*turn >= want) return true;
+      const uint64_t t0 = globaltimer_ns();
+      while (*turn < want) {
+        if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+        if (globaltimer_ns() - t0 > ctx.timeout_ns) {
+          atomicOr(ctx.status, kStatusTimeout);
+          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+          return false;
+        }
+      }
+      return true;
+    };
+    auto pass_turn = [&]() { *turn = 2 * m + (uint32_t)c + 1; };
+    // S_gg = Q K^T (A = Q in TMEM); releases (this thread's share of) the slots of K_gg and V_gg
+    auto issue_s = [&](uint32_t gg, bool pass) {
+      const uint32_t nk = 2 * gg;
+      const uint64_t b0 = sdesc_sw128(ring(nk), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+        mma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
+        if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
+      }
+      mma_commit(&ctl->bar_s_full);
+      mma_commit(&ctl->bar_kv_empty[nk % R]);
+      mma_commit(&ctl->bar_kv_empty[(nk + 1) % R]);
+    };
+    // dP_gg = dO V^T (A = dO in TMEM); V_gg is read only by this GEMM
+    auto issue_dp = [&](uint32_t gg, bool pass) {
+      const uint32_t nv = 2 * gg + 1;
+      const uint64_t b0 = sdesc_sw128(ring(nv), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+        mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
+        if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
+      }
+      mma_commit(&ctl->bar_dp_full);
+      mma_commit(&ctl->bar_kv_empty[nv % R]);
+    };
+    // dQ += dS K_gg (A = dS in the dP columns)
+    auto issue_dq = [&](uint32_t gg, bool first, bool pass) {
+      const uint32_t nk = 2 * gg;
+      const uint64_t b0 = sdesc_sw128(ring(nk), kChunkBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kBT / 16; ++kk) {
+        mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
+                    (!first || kk > 0) ? 1u : 0u);
+        if (pass && kk == kBT / 16 - 5) pass_turn();
+      }
+      mma_commit(&ctl->bar_kv_empty[nk % R]);
+    };
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
       // the key tiles of this item, in order (all lanes evaluate the same mask)
-      int j = 0;
       auto next_tile = [&](int from) {
         for (int jj = from; jj < nkt; ++jj)
           if (!kMask || key_tile_any(mask, w.b, S, jj)) return jj;
         return nkt;
       };
-      bool first = true;
-      // Q and dO of this item were stored into TMEM by the compute warps
-      if (lane == 0) ok = wait_or_abort(&ctl->bar_qdo_ready, it & 1, ctx, ctl);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      j = next_tile(0);
-      // Past the first key tile of an item the compute warps arrive on s_read /
-      // ds_ready only after they have seen K / V of the next tile land, so these
-      // MMAs need no wait of their own there: each wait of the issuing thread
-      // costs the tensor pipe a few hundred cycles (it queues only about one MMA).
-      auto issue_s = [&](uint32_t gg, bool wait) -> bool {
-        const uint32_t nk = 2 * gg;
-        if (wait && !wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl)) return false;
-        tc_fence_after();
-        const uint64_t b0 = sdesc_sw128(ring(nk), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
+      int j = next_tile(0);
+      if (j >= nkt) {
+        // no attended key: the compute warps write dQ = 0 once dq_done of the item arrives
+        if (lane == 0 && c == 1) mma_commit(&ctl->bar_dq_done);
+        __syncwarp();
+        continue;
+      }
+      if (lane == 0) {
+        // Q and dO of this item were stored into TMEM by the compute warps.  Past the
+        // first key tile the compute warps arrive on s_read / ds_ready only after they
+        // have seen K / V of the next tile land, so no other wait is needed.
+        ok = wait_or_abort(&ctl->bar_qdo_ready, it & 1, ctx, ctl);
+        if (ok) {
+          const uint32_t n0 = 2 * g + (uint32_t)c;  // K_g for chain s, V_g for chain d
+          ok = wait_or_abort(&ctl->bar_kv_full[n0 % R], (n0 / R) & 1, ctx, ctl);
         }
-        mma_commit(&ctl->bar_s_full);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t gg, bool wait) -> bool {
-        const uint32_t nv = 2 * gg + 1;
-        if (wait && !wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl)) return false;
-        tc_fence_after();
-        const uint64_t b0 = sdesc_sw128(ring(nv), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
-        }
-        mma_commit(&ctl->bar_dp_full);
-        mma_commit(&ctl->bar_kv_empty[nv % R]);  // V_j is only read by this dP
-        return true;
-      };
-      if (j < nkt) {
-        if (lane == 0) {
-          ok = issue_s(g, true);
-          if (ok) ok = issue_dp(g, true);
+        if (ok) ok = take_turn();
+        if (ok) {
+          tc_fence_after();
+          if (c == 0) issue_s(g, true);
+          else issue_dp(g, true);
+          ++m;
           mma_issued = true;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      bool first = true;
       while (ok && j < nkt) {
         const int jn = next_tile(j + 1);
         if (lane == 0) {
-          // S of the next key tile once this one's S was read into registers
-          if (jn < nkt) {
-            ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
+          if (c == 0) {
+            // S of the next key tile once this one's S was read into registers
+            if (jn < nkt) ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
+            if (ok) ok = take_turn();
             if (ok) {
               tc_fence_after();
-              ok = issue_s(g + 1, false);
+              if (jn < nkt) issue_s(g + 1, true);
+              else pass_turn();  // empty burst: keeps the two threads' burst counts equal
+            }
+          } else {
+            ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl);
+            if (ok && first && it > 0) ok = wait_or_abort(&ctl->bar_dq_free, (it - 1) & 1, ctx, ctl);
+            if (ok) ok = take_turn();
+            if (ok) {
+              tc_fence_after();
+              issue_dq(g, first, jn >= nkt);
+              if (jn < nkt) issue_dp(g + 1, true);
             }
           }
-          // dQ += dS K_j  (A = dS in the dP columns)
-          if (ok) ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl);
-          if (ok && first && it > 0) ok = wait_or_abort(&ctl->bar_dq_free, (it - 1) & 1, ctx, ctl);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t nk = 2 * g;
-            const uint64_t b0 = sdesc_sw128(ring(nk), kChunkBytes, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kBT / 16; ++kk)
-              mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
-                          (!first || kk > 0) ? 1u : 0u);
-            mma_commit(&ctl->bar_kv_empty[nk % R]);
-            // dP of the next key tile (dS was read by the dQ MMAs just issued)
-            if (jn < nkt) ok = issue_dp(g + 1, false);
-          }
+          ++m;
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         first = false;
@@ -829,9 +876,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&ctl->bar_dq_done);
+      if (lane == 0 && c == 1) mma_commit(&ctl->bar_dq_done);
       __syncwarp();
     }
+    if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer may wait for our turn
   } else {
     // ------------------------------------------------------------ compute warps 0..7
     const int qd = warp & 3;
@@ -975,9 +1023,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp && lane == 0 && mma_issued) {
-    mma_commit(&ctl->bar_final);
-    settle(&ctl->bar_final, 0, ctx);
+  if ((warp == kMmaWarp || warp == kMmaWarp1) && lane == 0 && mma_issued) {
+    mma_commit(&ctl->bar_final[warp - kMmaWarp]);
+    settle(&ctl->bar_final[warp - kMmaWarp], 0, ctx);
   }
   if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < R; ++s)
@@ -1041,7 +1089,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreadsDkdv, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
                                            static_cast<__nv_bfloat16*>(dv), S, H, (int)items, scale,
                                            scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
