@@ -15,8 +15,9 @@ Every step runs through the C ABI (``libuaa.so``).
 ``value`` = attention fwd+bwd FLOPs (4*B*H*S^2*D + 10*B*H*S^2*D) per second of
 the whole step (re-layouts included), inputs resident in HBM.  The inputs
 (4 x 279 MB) are larger than L2 (129 MB), so no L2 flush is added.  ``e2e``
-adds the host->device copy of the step's input shards from pinned memory and
-the device->host copy of O, dQ, dK, dV.  ``--impl reference`` times the fp64
+adds, every step, the host->device copy of the step's input shards from pinned
+memory and the device->host copy of O, dQ, dK, dV, on copy streams that overlap
+the compute where the data dependencies allow.  ``--impl reference`` times the fp64
 CPU oracle on bounded samples of the same workload instead.
 """
 from __future__ import annotations
@@ -334,15 +335,54 @@ def run_gpu(args, world, rank, local):
     step_flops = flops(B, S, H, D)
     value = world * step_flops / (ms * 1e-3) / 1e12
 
-    # e2e through the same public calls with host buffers: H2D of the input shards, D2H of O/dQ/dK/dV
+    # e2e through the same public calls with host buffers: every step copies its input shards (Q, K,
+    # V, dO) from pinned host memory and reads O, dQ, dK, dV back, inside the timed region.  The copies
+    # run on two copy streams ordered against the compute stream by events: dO arrives while the
+    # forward runs, O leaves while the backward runs, and the next step's Q, K, V arrive as soon as
+    # this step's seq->head exchange has consumed the previous ones (device buffers are reused).
     outs_host = {n: torch.empty_like(host["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    e_qkv_in, e_do_in, e_qkv_free, e_do_free, e_o_ready, e_g_ready, e_o_out, e_g_out = (
+        torch.cuda.Event() for _ in range(8))
+    for e in (e_qkv_free, e_do_free, e_o_out, e_g_out):
+        e.record(stream)
 
     def e2e_step():
-        for n in ("q", "k", "v", "do"):
-            sh[n].copy_(host[n], non_blocking=True)
-        step()
-        for n, t in (("o", o_sh), ("dq", dq_sh), ("dk", dk_sh), ("dv", dv_sh)):
-            outs_host[n].copy_(t, non_blocking=True)
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(e_qkv_free)
+            for n in ("q", "k", "v"):
+                sh[n].copy_(host[n], non_blocking=True)
+            e_qkv_in.record(h2d_s)
+            h2d_s.wait_event(e_do_free)
+            sh["do"].copy_(host["do"], non_blocking=True)
+            e_do_in.record(h2d_s)
+        stream.wait_event(e_qkv_in)
+        for n, y in (("q", yq), ("k", yk), ("v", yv)):
+            uaa.seq_to_head(sh[n], lens, out=y)
+        e_qkv_free.record(stream)
+        uaa.attn_fwd(yq.view(P * B, S, Hg, D), yk.view(P * B, S, Hg, D), yv.view(P * B, S, Hg, D), None, w.scale,
+                     out=yo.view(P * B, S, Hg, D), lse=lse.view(P * B, Hg, S))
+        stream.wait_event(e_o_out)  # the previous step's read-back of O is done with o_sh
+        uaa.head_to_seq(yo, lens, cap, out=o_sh)
+        e_o_ready.record(stream)
+        stream.wait_event(e_do_in)
+        uaa.seq_to_head(sh["do"], lens, out=ydo)
+        e_do_free.record(stream)
+        g4 = lambda t: t.view(P * B, S, Hg, D)  # noqa: E731
+        uaa.attn_bwd(g4(yq), g4(yk), g4(yv), g4(yo), g4(ydo), lse.view(P * B, Hg, S), None, w.scale, dq=g4(ydq),
+                     dk=g4(ydk), dv=g4(ydv), workspace=ws)
+        stream.wait_event(e_g_out)  # the previous step's read-back of the gradients is done
+        for y, x in ((ydq, dq_sh), (ydk, dk_sh), (ydv, dv_sh)):
+            uaa.head_to_seq(y, lens, cap, out=x)
+        e_g_ready.record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(e_o_ready)
+            outs_host["o"].copy_(o_sh, non_blocking=True)
+            e_o_out.record(d2h_s)
+            d2h_s.wait_event(e_g_ready)
+            for n, t in (("dq", dq_sh), ("dk", dk_sh), ("dv", dv_sh)):
+                outs_host[n].copy_(t, non_blocking=True)
+            e_g_out.record(d2h_s)
 
     e2e = None
     if not args.no_e2e:
@@ -352,15 +392,20 @@ def run_gpu(args, world, rank, local):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        h2d_s.wait_event(e0)
+        d2h_s.wait_event(e0)
         for _ in range(args.steps):
             e2e_step()
+        stream.wait_stream(h2d_s)
+        stream.wait_stream(d2h_s)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
         e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "copies": "two copy streams overlapped with compute (event-ordered)"}
     uaa.check_device_status(dev)
 
     pk, src = peaks()
