@@ -147,10 +147,11 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, x):
+def max_over_ranks(world, x, device="cuda"):
+    """The slowest rank's time: every rank gets the maximum of ``x`` over the process group."""
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        t = torch.tensor([x], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
     return x
