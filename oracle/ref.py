@@ -260,21 +260,25 @@ def unshard_sequence(shards, shard_lens):
 
 
 def seq_to_head(x, shard_lens, cap):
-    """Forward Ulysses exchange: ``(P, B, cap, H, D)`` shards -> ``(P, B, N, H/P, D)`` groups.
+    """Forward Ulysses exchange: ``(P, B, cap, H, D)`` shards -> ``(P, B, N, Hg, D)`` groups.
 
-    ``y[g, b, off_p + s, h', :] = x[p, b, s, g*H/P + h', :]`` for ``s < L_p``:
+    ``Hg = ceil(H / P)``.  ``y[g, b, off_p + s, h', :] = x[p, b, s, g*Hg + h', :]``
+    for ``s < L_p`` and ``g*Hg + h' < H``; heads ``g*Hg + h' >= H`` are zero:
     every rank sends head group g of its shard to rank g, which concatenates the
     shards it receives in rank order, trimmed to their true lengths ("UAA-bwd",
     What does this PR do: reuse of the all-to-all helpers with the saved
-    partition metadata).
+    partition metadata; the head dimension is padded with zero heads to a
+    multiple of P when P does not divide H -- the padded-head layouts of Ulysses
+    Anything, "UAA-bwd", What does this PR do and Tests).
     """
     P, B, C, H, D = x.shape
     lens, _ = _offsets(shard_lens)
     if len(lens) != P or C != cap:
         raise ValueError("shard buffer does not match shard_lens / cap")
-    if H % P:
-        raise ValueError("H must be divisible by P (padded heads are not implemented)")
-    hg = H // P
+    hg = -(-H // P)
+    if hg * P != H:
+        pad = np.zeros((P, B, C, hg * P - H, D), dtype=x.dtype)
+        x = np.concatenate([x, pad], axis=3)
     groups = []
     for g in range(P):
         parts = [x[p, :, :lens[p], g * hg:(g + 1) * hg, :] for p in range(P)]
@@ -282,12 +286,13 @@ def seq_to_head(x, shard_lens, cap):
     return np.stack(groups, axis=0)
 
 
-def head_to_seq(y, shard_lens, cap):
-    """Inverse Ulysses exchange: ``(P, B, N, H/P, D)`` groups -> ``(P, B, cap, H, D)`` shards.
+def head_to_seq(y, shard_lens, cap, H=None):
+    """Inverse Ulysses exchange: ``(P, B, N, Hg, D)`` groups -> ``(P, B, cap, H, D)`` shards.
 
-    Rows ``s >= L_p`` of shard p (transport padding) are zero.  "UAA-bwd", What
-    does this PR do: the outputs and the Q/K/V gradients are restored to the
-    sequence-sharded layout by the inverse all-to-all.
+    Rows ``s >= L_p`` of shard p (transport padding) are zero; the zero padding
+    heads (``H < P*Hg``) are dropped.  ``H`` defaults to ``P*Hg``.  "UAA-bwd",
+    What does this PR do: the outputs and the Q/K/V gradients are restored to
+    the sequence-sharded layout by the inverse all-to-all.
     """
     P, B, N, hg, D = y.shape
     lens, offs = _offsets(shard_lens)
@@ -295,11 +300,14 @@ def head_to_seq(y, shard_lens, cap):
         raise ValueError("group buffer does not match shard_lens")
     if max(lens) > cap:
         raise ValueError("a shard is longer than the capacity")
+    H = P * hg if H is None else int(H)
+    if not ((hg - 1) * P < H <= P * hg):
+        raise ValueError("H does not match the group size")
     x = np.zeros((P, B, cap, P * hg, D), dtype=y.dtype)
     for p in range(P):
         for g in range(P):
             x[p, :, :lens[p], g * hg:(g + 1) * hg, :] = y[g, :, offs[p]:offs[p] + lens[p]]
-    return x
+    return x[:, :, :, :H]
 
 
 def split_key_mask(mask, shard_lens, cap):
@@ -336,9 +344,10 @@ def ulysses_attn_fwd(q_sh, k_sh, v_sh, shard_lens, cap, mask_sh=None, scale=None
 
     seq->head exchange of Q/K/V, attention per head group (the mask, gathered
     from its shards and trimmed, is shared by all heads), head->seq exchange
-    of O.  LSE is returned head-sharded ``(P, B, H/P, N)``, as each rank keeps
-    it.  "UAA-bwd", What does this PR do.
+    of O.  LSE is returned head-sharded ``(P, B, Hg, N)``, as each rank keeps
+    it (rows of padding heads included).  "UAA-bwd", What does this PR do.
     """
+    H = q_sh.shape[3]
     yq = seq_to_head(q_sh, shard_lens, cap)
     yk = seq_to_head(k_sh, shard_lens, cap)
     yv = seq_to_head(v_sh, shard_lens, cap)
@@ -349,7 +358,7 @@ def ulysses_attn_fwd(q_sh, k_sh, v_sh, shard_lens, cap, mask_sh=None, scale=None
         o, lse = attn_fwd(yq[g], yk[g], yv[g], mask, scale)
         outs.append(o)
         lses.append(lse)
-    return head_to_seq(np.stack(outs), shard_lens, cap), np.stack(lses)
+    return head_to_seq(np.stack(outs), shard_lens, cap, H), np.stack(lses)
 
 
 def ulysses_attn_bwd(q_sh, k_sh, v_sh, do_sh, shard_lens, cap, mask_sh=None, scale=None):
@@ -360,6 +369,7 @@ def ulysses_attn_bwd(q_sh, k_sh, v_sh, do_sh, shard_lens, cap, mask_sh=None, sca
     here, so both partitions are ``shard_lens``).  "UAA-bwd", What does this
     PR do.
     """
+    H = q_sh.shape[3]
     yq = seq_to_head(q_sh, shard_lens, cap)
     yk = seq_to_head(k_sh, shard_lens, cap)
     yv = seq_to_head(v_sh, shard_lens, cap)
@@ -372,6 +382,6 @@ def ulysses_attn_bwd(q_sh, k_sh, v_sh, do_sh, shard_lens, cap, mask_sh=None, sca
         dqs.append(dq)
         dks.append(dk)
         dvs.append(dv)
-    return (head_to_seq(np.stack(dqs), shard_lens, cap),
-            head_to_seq(np.stack(dks), shard_lens, cap),
-            head_to_seq(np.stack(dvs), shard_lens, cap))
+    return (head_to_seq(np.stack(dqs), shard_lens, cap, H),
+            head_to_seq(np.stack(dks), shard_lens, cap, H),
+            head_to_seq(np.stack(dvs), shard_lens, cap, H))

@@ -235,6 +235,50 @@ def test_relayout_is_a_bijection_and_round_trips(lens, cap):
     np.testing.assert_array_equal(oracle.unshard_sequence(back, lens), full)
 
 
+@pytest.mark.parametrize("H,P", [(6, 4), (5, 2), (3, 4)])
+def test_relayout_padded_heads(H, P):
+    """H % P != 0: heads are zero-padded to P*ceil(H/P) on the way in and dropped on the way back."""
+    lens = tuple([4, 3, 4, 2][:P]) if P <= 4 else None
+    cap = max(lens)
+    B, D = 2, 3
+    N = sum(lens)
+    hg = -(-H // P)
+    full = np.arange(B * N * H * D, dtype=np.float64).reshape(B, N, H, D) + 1.0
+    x = oracle.shard_sequence(full, lens, cap)
+    y = oracle.seq_to_head(x, lens, cap)
+    assert y.shape == (P, B, N, hg, D)
+    for g in range(P):
+        for hh in range(hg):
+            h = g * hg + hh
+            if h < H:
+                np.testing.assert_array_equal(y[g, :, :, hh], full[:, :, h])
+            else:
+                assert (y[g, :, :, hh] == 0).all()      # padding head
+    nz = y[y != 0]
+    assert nz.size == full.size and len(np.unique(nz)) == full.size  # each real element exactly once
+    back = oracle.head_to_seq(y, lens, cap, H)
+    assert back.shape == x.shape
+    np.testing.assert_array_equal(back, x)
+
+
+def test_ulysses_composition_with_padded_heads():
+    lens, cap = (5, 4, 4, 3), 5
+    B, N, H, D = 1, 16, 6, 8
+    q, k, v, do = (rnd((B, N, H, D), s + 10) for s in range(4))
+    sh = [oracle.shard_sequence(t, lens, cap) for t in (q, k, v, do)]
+    o_sh, lse_g = oracle.ulysses_attn_fwd(sh[0], sh[1], sh[2], lens, cap)
+    o, lse = oracle.attn_fwd(q, k, v)
+    np.testing.assert_allclose(oracle.unshard_sequence(o_sh, lens), o, atol=1e-14)
+    assert lse_g.shape == (4, B, 2, N)
+    for h in range(H):
+        np.testing.assert_allclose(lse_g[h // 2][:, h % 2], lse[:, h], atol=1e-14)
+    np.testing.assert_allclose(lse_g[3], np.log(N), atol=1e-14)  # zero heads: uniform over all keys
+    dq_sh, dk_sh, dv_sh = oracle.ulysses_attn_bwd(*sh, lens, cap)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do)
+    for a, b in ((dq_sh, dq), (dk_sh, dk), (dv_sh, dv)):
+        np.testing.assert_allclose(oracle.unshard_sequence(a, lens), b, atol=1e-13)
+
+
 def test_relayout_matches_synth_padding():
     lens, cap = (5, 5, 4, 3), 5
     full = torch.arange(2 * 17 * 4 * 2, dtype=torch.float32).reshape(2, 17, 4, 2)
