@@ -53,7 +53,7 @@ typedef void* uaa_stream_t;
 typedef enum {
   UAA_OK = 0,
   UAA_ERR_INVALID_ARG = -1,   /* bad pointer, size, shape or alignment */
-  UAA_ERR_UNSUPPORTED = -2,   /* valid request outside what is built (D not 64/128, H % P != 0) */
+  UAA_ERR_UNSUPPORTED = -2,   /* valid request outside what is built (e.g. D not 64/128) */
   UAA_ERR_PER_HEAD_MASK = -3, /* a (B, H>1, 1, S) mask: Ulysses cannot shard it ("UAA-bwd",
                                  What does this PR do: fail fast on per-head masks) */
   UAA_ERR_CUDA = -4,          /* a CUDA runtime / driver call failed */
@@ -143,21 +143,24 @@ size_t uaa_attn_bwd_noalloc_max_bytes(void);
  * uneven shards); "fast-ulysses", Summary (A2A around the attention module).
  *   x : device (P, B, cap, H, D) -- shard p's rows s < shard_lens[p] are valid,
  *       rows s >= shard_lens[p] are transport padding (not read)
- *   y : device (P, B, N, H/P, D), N = sum(shard_lens); group g holds heads
- *       [g*H/P, (g+1)*H/P) of every valid row, shards concatenated in rank order:
- *       y[g, b, off_p + s, h', :] = x[p, b, s, g*H/P + h', :]
+ *   y : device (P, B, N, Hg, D), Hg = ceil(H/P), N = sum(shard_lens); group g
+ *       holds heads [g*Hg, (g+1)*Hg) of every valid row, shards concatenated in
+ *       rank order: y[g, b, off_p + s, h', :] = x[p, b, s, g*Hg + h', :]; heads
+ *       g*Hg + h' >= H are zero (padded-head layout when P does not divide H,
+ *       "UAA-bwd", What does this PR do)
  *   shard_lens : host, P ints, 0 <= shard_lens[p] <= cap
  *   elem_bytes : bytes per element (2 for bf16, 4 for fp32); D*elem_bytes must
  *       be a multiple of 16
- * H % P != 0 (padded heads) returns UAA_ERR_UNSUPPORTED.  x and y must not
- * overlap.  Bit-exact copy. */
+ * x and y must not overlap.  Bit-exact copy. */
 int uaa_seq_to_head(const void* x, void* y, int P, const int* shard_lens, int cap,
                     int B, int H, int D, int elem_bytes, uaa_stream_t stream);
 
 /* Ulysses inverse exchange: head groups -> sequence shards (exact inverse of
- * uaa_seq_to_head).  Padding rows s >= shard_lens[p] of every shard are
- * written as zero.  Used for O in the forward and for dQ (query partition) and
- * dK/dV (key partition) in the backward ("UAA-bwd", What does this PR do). */
+ * uaa_seq_to_head).  y is (P, B, N, ceil(H/P), D), x is (P, B, cap, H, D) with
+ * the true head count H: the padding heads of the groups are dropped.  Padding
+ * rows s >= shard_lens[p] of every shard are written as zero.  Used for O in the
+ * forward and for dQ (query partition) and dK/dV (key partition) in the backward
+ * ("UAA-bwd", What does this PR do). */
 int uaa_head_to_seq(const void* y, void* x, int P, const int* shard_lens, int cap,
                     int B, int H, int D, int elem_bytes, uaa_stream_t stream);
 

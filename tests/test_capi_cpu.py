@@ -77,8 +77,8 @@ def test_relayout_rejects_bad_partitions_on_host(L):
     P = ctypes.c_void_p
     fake = P(1 << 20)
     lens = (ctypes.c_int * 4)(6821, 6821, 6819, 6819)
-    # H % P != 0: padded heads are not built
-    assert L.uaa_seq_to_head(fake, fake, 4, lens, 6821, 1, 42, 128, 2, None) == -2
+    # P outside [1, 64]
+    assert L.uaa_seq_to_head(fake, fake, 0, lens, 6821, 1, 40, 128, 2, None) == -1
     # a shard longer than the capacity
     assert L.uaa_seq_to_head(fake, fake, 4, lens, 6820, 1, 40, 128, 2, None) == -1
     assert "cap" in _err()

@@ -193,6 +193,41 @@ def test_ulysses_emulation_workload():
     compare("ulysses dV", f64(unshard(v_sh.grad))[:, :, h], rdv, "dv")
 
 
+def test_ulysses_padded_heads_equal_the_unsharded_path():
+    """P = 4 does not divide H = 6: the head groups carry zero padding heads.
+
+    Attention on a zero head is well defined (uniform weights, O = 0, zero
+    gradients) and the padding heads are dropped on the way back, so the real
+    heads' O, LSE and gradients equal the unsharded path bit for bit.
+    """
+    lens, cap = (301, 300, 257, 130), 301
+    B, H, D = 2, 6, 128
+    inp = synth.draw(B, sum(lens), H, D, seed=31)
+    scale = 1.0 / np.sqrt(D)
+    sh = {n: synth.pad_shards(inp[n], lens, cap).to(DEV) for n in ("q", "k", "v", "do")}
+    q_sh = sh["q"].requires_grad_(True)
+    k_sh = sh["k"].requires_grad_(True)
+    v_sh = sh["v"].requires_grad_(True)
+    o_sh, lse_g = uaa.ulysses_attention(q_sh, k_sh, v_sh, lens, None, scale)
+    o_sh.backward(sh["do"])
+    uaa.check_device_status()
+    assert tuple(o_sh.shape) == (4, B, cap, H, D) and tuple(lse_g.shape) == (4, B, 2, sum(lens))
+    o, lse, dq, dk, dv = run_gpu(inp, scale, None)
+
+    def unshard(t):
+        return torch.cat([t[p, :, :L] for p, L in enumerate(lens)], dim=1)
+
+    assert np.array_equal(bits(unshard(o_sh.detach())), bits(o))
+    for h in range(H):
+        assert np.array_equal(bits(lse_g[h // 2][:, h % 2]), bits(lse[:, h]))
+    assert np.array_equal(bits(unshard(q_sh.grad)), bits(dq))
+    assert np.array_equal(bits(unshard(k_sh.grad)), bits(dk))
+    assert np.array_equal(bits(unshard(v_sh.grad)), bits(dv))
+    for p, L in enumerate(lens):
+        for t in (o_sh, q_sh.grad, k_sh.grad, v_sh.grad):
+            assert (bits(t[p, :, L:]) == 0).all()
+
+
 def test_autograd_function_marks_lse_non_differentiable():
     inp = synth.draw(1, 64, 2, 64, seed=9)
     q, k, v = (inp[n].to(DEV).requires_grad_(True) for n in ("q", "k", "v"))

@@ -1,8 +1,9 @@
 """GPU re-layout and mask-assembly kernels vs the oracle, bit for bit.
 
 Covers even and uneven (Ulysses Anything) partitions, an empty shard, P = 1,
-D = 64/128, fp32 elements, the zeroed transport padding, and the full
-N = 27280, H = 40, D = 128 workload with shards (6821, 6821, 6819, 6819).
+D = 64/128, fp32 elements, the zeroed transport padding, padded heads
+(P does not divide H), and the full N = 27280, H = 40, D = 128 workload with
+shards (6821, 6821, 6819, 6819).
 """
 import numpy as np
 import pytest
@@ -32,6 +33,10 @@ CASES = [
     (1, (1, 9, 0, 4), 9, 4, 128, torch.bfloat16),
     (3, (33,), 40, 6, 64, torch.bfloat16),
     (2, (5, 3), 5, 4, 64, torch.float32),
+    # padded heads: P does not divide H
+    (2, (7, 7, 5, 5), 8, 6, 64, torch.bfloat16),
+    (1, (5, 3, 4), 5, 8, 128, torch.bfloat16),
+    (1, (6821, 6821, 6819, 6819), 6821, 42, 128, torch.bfloat16),
 ]
 
 
@@ -41,17 +46,21 @@ def test_seq_to_head_and_back_bit_exact(B, lens, cap, H, D, dtype):
     xd = x.to(DEV)
     y = uaa.seq_to_head(xd, lens)
     back = torch.full_like(xd, float("nan"))  # padding must be overwritten with zeros
-    uaa.head_to_seq(y, lens, cap, out=back)
+    uaa.head_to_seq(y, lens, cap, H, out=back)
     uaa.check_device_status()
     xb = bits(x)
     np.testing.assert_array_equal(bits(y), oracle.seq_to_head(xb, lens, cap))
-    np.testing.assert_array_equal(bits(back), oracle.head_to_seq(oracle.seq_to_head(xb, lens, cap), lens, cap))
+    np.testing.assert_array_equal(bits(back), oracle.head_to_seq(oracle.seq_to_head(xb, lens, cap), lens, cap, H))
     np.testing.assert_array_equal(bits(back), xb)  # round trip, padding rows zero
-    # the head groups are the head slices of the unsharded sequence
+    # the head groups are the head slices of the unsharded sequence, padding heads zero
     P = len(lens)
+    hg = -(-H // P)
+    assert y.shape[3] == hg
     fb = bits(full)
     for g in range(P):
-        np.testing.assert_array_equal(bits(y[g]), fb[:, :, g * (H // P):(g + 1) * (H // P)])
+        real = max(0, min(hg, H - g * hg))
+        np.testing.assert_array_equal(bits(y[g, :, :, :real]), fb[:, :, g * hg:g * hg + real])
+        assert (bits(y[g, :, :, real:]) == 0).all()
 
 
 def test_head_to_seq_of_arbitrary_groups_matches_oracle():

@@ -216,7 +216,10 @@ def _lens_array(shard_lens):
 
 
 def seq_to_head(x, shard_lens, out=None):
-    """``uaa_seq_to_head``: ``(P, B, cap, H, D)`` shards -> ``(P, B, N, H/P, D)`` groups."""
+    """``uaa_seq_to_head``: ``(P, B, cap, H, D)`` shards -> ``(P, B, N, ceil(H/P), D)`` groups.
+
+    When P does not divide H the groups are padded with zero heads.
+    """
     _need_cuda(x)
     if x.dim() != 5 or not x.is_contiguous():
         raise ValueError("x must be contiguous (P, B, cap, H, D)")
@@ -224,27 +227,31 @@ def seq_to_head(x, shard_lens, out=None):
     arr, lens = _lens_array(shard_lens)
     if len(lens) != P:
         raise ValueError("len(shard_lens) must equal P")
-    if H % P:
-        raise ValueError(f"H={H} must be divisible by P={P} (padded heads are not implemented)")
     N = sum(lens)
     if out is None:
-        out = torch.empty((P, B, N, H // P, D), dtype=x.dtype, device=x.device)
+        out = torch.empty((P, B, N, -(-H // P), D), dtype=x.dtype, device=x.device)
     _check(lib().uaa_seq_to_head(_ptr(x), _ptr(out), P, arr, cap, B, H, D, x.element_size(), _P(_stream(x.device))))
     return out
 
 
-def head_to_seq(y, shard_lens, cap, out=None):
-    """``uaa_head_to_seq``: ``(P, B, N, H/P, D)`` groups -> ``(P, B, cap, H, D)`` shards (padding zeroed)."""
+def head_to_seq(y, shard_lens, cap, H=None, out=None):
+    """``uaa_head_to_seq``: ``(P, B, N, Hg, D)`` groups -> ``(P, B, cap, H, D)`` shards (padding zeroed).
+
+    ``H`` is the true head count (default ``P * Hg``); padding heads of the groups are dropped.
+    """
     _need_cuda(y)
     if y.dim() != 5 or not y.is_contiguous():
-        raise ValueError("y must be contiguous (P, B, N, H/P, D)")
+        raise ValueError("y must be contiguous (P, B, N, Hg, D)")
     P, B, N, Hg, D = y.shape
+    H = P * Hg if H is None else int(H)
+    if not (Hg - 1) * P < H <= Hg * P:
+        raise ValueError(f"H={H} does not have ceil(H/P) = {Hg} heads per group")
     arr, lens = _lens_array(shard_lens)
     if len(lens) != P or sum(lens) != N:
         raise ValueError("shard_lens must have P entries summing to N")
     if out is None:
-        out = torch.empty((P, B, cap, Hg * P, D), dtype=y.dtype, device=y.device)
-    _check(lib().uaa_head_to_seq(_ptr(y), _ptr(out), P, arr, cap, B, Hg * P, D, y.element_size(),
+        out = torch.empty((P, B, cap, H, D), dtype=y.dtype, device=y.device)
+    _check(lib().uaa_head_to_seq(_ptr(y), _ptr(out), P, arr, cap, B, H, D, y.element_size(),
                                  _P(_stream(y.device))))
     return out
 
@@ -307,7 +314,7 @@ class UlyssesAttention(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):
-        cap = q_sh.shape[2]
+        cap, H = q_sh.shape[2], q_sh.shape[3]
         yq, yk, yv = (seq_to_head(t, shard_lens) for t in (q_sh, k_sh, v_sh))
         P = yq.shape[0]
         o = torch.empty_like(yq)
@@ -318,9 +325,9 @@ class UlyssesAttention(torch.autograd.Function):
         else:
             for g in range(P):
                 attn_fwd(yq[g], yk[g], yv[g], key_mask, scale, out=o[g], lse=lse[g])
-        o_sh = head_to_seq(o, shard_lens, cap)
+        o_sh = head_to_seq(o, shard_lens, cap, H)
         ctx.save_for_backward(yq, yk, yv, o, lse)
-        ctx.shard_lens, ctx.key_mask, ctx.scale, ctx.cap = tuple(shard_lens), key_mask, scale, cap
+        ctx.shard_lens, ctx.key_mask, ctx.scale, ctx.cap, ctx.H = tuple(shard_lens), key_mask, scale, cap, H
         ctx.mark_non_differentiable(lse)
         return o_sh, lse
 
@@ -338,8 +345,8 @@ class UlyssesAttention(torch.autograd.Function):
             for g in range(P):
                 attn_bwd(yq[g], yk[g], yv[g], o[g], ydo[g], lse[g], ctx.key_mask, ctx.scale, dq=dq[g], dk=dk[g],
                          dv=dv[g], workspace=ws)
-        return (head_to_seq(dq, ctx.shard_lens, ctx.cap), head_to_seq(dk, ctx.shard_lens, ctx.cap),
-                head_to_seq(dv, ctx.shard_lens, ctx.cap), None, None, None)
+        return (head_to_seq(dq, ctx.shard_lens, ctx.cap, ctx.H), head_to_seq(dk, ctx.shard_lens, ctx.cap, ctx.H),
+                head_to_seq(dv, ctx.shard_lens, ctx.cap, ctx.H), None, None, None)
 
 
 def ulysses_attention(q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):

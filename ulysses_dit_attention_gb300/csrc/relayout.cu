@@ -36,7 +36,8 @@ __device__ __forceinline__ int find_shard(const Partition& part, int n) {
   return p;
 }
 
-// y[g, b, n, h', :] = x[p, b, s, g*Hg + h', :] with n = offs[p] + s.
+// y[g, b, n, h', :] = x[p, b, s, g*Hg + h', :] with n = offs[p] + s, and 0 for
+// the padding heads g*Hg + h' >= H (Hg = ceil(H/P)).
 // Index space = output vectors, in output order (g, b, n, h', v).
 __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const uint4* __restrict__ x, uint4* __restrict__ y,
                                                                const __grid_constant__ Partition part, int B,
@@ -60,8 +61,11 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const uint4* __re
         const int g = (int)(r / (uint32_t)B);
         const int p = find_shard(part, n);
         const int s = n - part.offs[p];
-        const size_t src = (((size_t)p * B + b) * part.cap + s) * (size_t)H * rowvec + (size_t)g * run + w;
-        v[u] = __ldcs(x + src);
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if ((uint32_t)g * run + w < (uint32_t)H * rowvec) {  // a real head, not padding
+          const size_t src = (((size_t)p * B + b) * part.cap + s) * (size_t)H * rowvec + (size_t)g * run + w;
+          v[u] = __ldcs(x + src);
+        }
       }
     }
 #pragma unroll
@@ -70,8 +74,9 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const uint4* __re
   }
 }
 
-// x[p, b, s, h, :] = y[h / Hg, b, offs[p] + s, h % Hg, :] for s < L_p, else 0.
-// Index space = output vectors, in output order (p, b, s, h, v), padding included.
+// x[p, b, s, h, :] = y[h / Hg, b, offs[p] + s, h % Hg, :] for s < L_p, else 0
+// (h < H only: the padding heads of the groups are dropped).
+// Index space = output vectors, in output order (p, b, s, h, v), padding rows included.
 __global__ void __launch_bounds__(kThreads) head_to_seq_kernel(const uint4* __restrict__ y, uint4* __restrict__ x,
                                                                const __grid_constant__ Partition part, int B,
                                                                int H, int Hg, int rowvec, uint32_t total) {
@@ -181,10 +186,10 @@ int relayout_common(const char* fn, const void* src, const void* dst, int P, con
   if (((int64_t)D * elem_bytes) % 16)
     return set_error(UAA_ERR_INVALID_ARG, "%s: D*elem_bytes=%lld is not a multiple of 16", fn,
                      (long long)D * elem_bytes);
-  if (H % P) return set_error(UAA_ERR_UNSUPPORTED, "%s: H=%d is not divisible by P=%d (padded heads)", fn, H, P);
   *rowvec = (int)((int64_t)D * elem_bytes / 16);
-  *Hg = H / P;
-  const uint64_t big = (uint64_t)P * B * (uint64_t)(cap > part->offs[P] ? cap : part->offs[P]) * H * (*rowvec);
+  *Hg = (H + P - 1) / P;  // P does not have to divide H: the groups are padded with zero heads
+  const uint64_t big =
+      (uint64_t)P * B * (uint64_t)(cap > part->offs[P] ? cap : part->offs[P]) * ((uint64_t)P * (*Hg)) * (*rowvec);
   if (big >= (1ull << 31)) return set_error(UAA_ERR_UNSUPPORTED, "%s: tensor too large (>= 2^31 16-byte vectors)", fn);
   if (B == 0) return UAA_OK;
   if ((st = check_ptr(fn, "src", src, 16))) return st;
@@ -205,7 +210,7 @@ int uaa_seq_to_head(const void* x, void* y, int P, const int* shard_lens, int ca
   int rowvec = 0, Hg = 0;
   int st = relayout_common("uaa_seq_to_head", x, y, P, shard_lens, cap, B, H, D, elem_bytes, &part, &rowvec, &Hg);
   if (st) return st;
-  const uint32_t total = (uint32_t)((uint64_t)B * part.offs[P] * H * rowvec);
+  const uint32_t total = (uint32_t)((uint64_t)P * B * part.offs[P] * Hg * rowvec);
   if (total == 0) return UAA_OK;
   seq_to_head_kernel<<<grid_for(total, kUnroll), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(x), static_cast<uint4*>(y), part, B, H, Hg, rowvec, total);
