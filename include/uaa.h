@@ -75,6 +75,20 @@ int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key
                  void* out, float* lse, int B, int S, int H, int D, float scale,
                  uaa_stream_t stream);
 
+/* Attention forward with separate query and key lengths (cross-attention, or a
+ * query block against a key set of another length).  "UAA-bwd", What does
+ * this PR do: the query and key partition metadata are saved separately, so
+ * the query and key sequences can be sharded -- and be as long -- differently.
+ *   q        : device, bf16 (B, Sq, H, D)
+ *   k, v     : device, bf16 (B, Sk, H, D)
+ *   key_mask : device, uint8 (B, Sk) or NULL
+ *   out      : device, bf16 (B, Sq, H, D); lse : device, fp32 (B, H, Sq)
+ * Sk must be positive when Sq is.  uaa_attn_fwd(..., S, ...) is this call with
+ * Sq = Sk = S.  Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_fwd_cross(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                       void* out, float* lse, int B, int Sq, int Sk, int H, int D, float scale,
+                       uaa_stream_t stream);
+
 /* Bytes of device workspace uaa_attn_bwd needs for (B, S, H, D): two fp32
  * (B, H, S_pad) vectors, S_pad = S rounded up to a multiple of 128 -- the row
  * dot Delta = rowsum(dO * O) and -LSE * log2(e) -- rounded up to 256 bytes.
@@ -98,6 +112,19 @@ int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                  const void* dout, const float* lse, const uint8_t* key_mask,
                  void* dq, void* dk, void* dv, int B, int S, int H, int D, float scale,
                  void* workspace, size_t workspace_bytes, uaa_stream_t stream);
+
+/* Attention backward with separate query and key lengths (the backward of
+ * uaa_attn_fwd_cross; "UAA-bwd", What does this PR do: dQ follows the query
+ * partition, dK/dV the key partition).
+ *   q, out, dout, dq : device, bf16 (B, Sq, H, D); lse : fp32 (B, H, Sq)
+ *   k, v, dk, dv     : device, bf16 (B, Sk, H, D); key_mask : uint8 (B, Sk) or NULL
+ *   workspace        : at least uaa_attn_bwd_workspace_bytes(B, Sq, H, D) bytes
+ * Sq and Sk must both be positive (or B*H = 0).  uaa_attn_bwd(..., S, ...) is
+ * this call with Sq = Sk = S.  Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_bwd_cross(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, const uint8_t* key_mask,
+                       void* dq, void* dk, void* dv, int B, int Sq, int Sk, int H, int D,
+                       float scale, void* workspace, size_t workspace_bytes, uaa_stream_t stream);
 
 /* Profiling aid (off by default; the pages have no counterpart): when the
  * three CUDA events (cudaEvent_t, created by the caller) are non-NULL, every

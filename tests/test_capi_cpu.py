@@ -90,6 +90,21 @@ def test_relayout_rejects_bad_partitions_on_host(L):
     assert L.uaa_watchdog_selftest(0, None) == -1
 
 
+def test_cross_attention_rejects_missing_sides_on_host(L):
+    fake = ctypes.c_void_p(1 << 20)
+    # queries without keys
+    assert L.uaa_attn_fwd_cross(fake, fake, fake, None, fake, fake, 1, 128, 0, 2, 128, ctypes.c_float(0.1),
+                                None) == -1
+    assert "Sk" in _err()
+    # keys without queries in the backward
+    assert L.uaa_attn_bwd_cross(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, 1, 0, 128, 2, 128,
+                                ctypes.c_float(0.1), fake, 1 << 20, None) == -1
+    assert "Sq" in _err()
+    # nothing to do: no queries in the forward
+    assert L.uaa_attn_fwd_cross(fake, fake, fake, None, fake, fake, 1, 0, 128, 2, 128, ctypes.c_float(0.1),
+                                None) == 0
+
+
 def test_python_binding_rejects_per_head_mask_before_launch():
     import torch
     with pytest.raises(ValueError, match="per-head"):

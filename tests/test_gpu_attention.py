@@ -193,6 +193,51 @@ def test_ulysses_emulation_workload():
     compare("ulysses dV", f64(unshard(v_sh.grad))[:, :, h], rdv, "dv")
 
 
+CROSS = [
+    # B, Sq, Sk, H, D, masked
+    (2, 300, 700, 3, 128, True),    # more keys than queries, ragged tiles, key mask (B, Sk)
+    (1, 1000, 257, 2, 64, False),   # more queries than keys
+    (1, 128, 1, 2, 128, False),     # a single key
+]
+
+
+@pytest.mark.parametrize("B,Sq,Sk,H,D,masked", CROSS)
+def test_cross_attention_sq_ne_sk(B, Sq, Sk, H, D, masked):
+    """Separate query and key lengths ("[attention] Add Ulysses Anything backward", What does
+    this PR do: query and key partition metadata are kept separately)."""
+    g = torch.Generator().manual_seed(Sq * 7 + Sk)
+    q = torch.randn((B, Sq, H, D), generator=g).to(torch.bfloat16)
+    k, v = (torch.randn((B, Sk, H, D), generator=g).to(torch.bfloat16) for _ in range(2))
+    do = torch.randn((B, Sq, H, D), generator=g).to(torch.bfloat16)
+    mask = None
+    if masked:
+        lens = torch.randint(Sk // 2, Sk + 1, (B,), generator=g)
+        mask = (torch.arange(Sk)[None, :] < lens[:, None]).to(torch.uint8)
+    scale = 1.0 / np.sqrt(D)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    md = None if mask is None else mask.to(DEV)
+    o, lse = uaa.attn_fwd(qd, kd, vd, md, scale)
+    dq, dk, dv = uaa.attn_bwd(qd, kd, vd, o, dod, lse, md, scale)
+    uaa.check_device_status()
+    assert tuple(o.shape) == (B, Sq, H, D) and tuple(lse.shape) == (B, H, Sq)
+    assert tuple(dq.shape) == (B, Sq, H, D) and tuple(dk.shape) == (B, Sk, H, D)
+    m = None if mask is None else mask.numpy().astype(bool)
+    qq, kk, vv, dd = (f64(t) for t in (q, k, v, do))
+    ro, rl = oracle.attn_fwd(qq, kk, vv, m, scale)
+    rdq, rdk, rdv = oracle.attn_bwd(qq, kk, vv, dd, m, scale)
+    # with a single key every query puts weight 1 on it: dV is a sum of Sq rows of dO (|dV| ~ sqrt(Sq)),
+    # so the absolute bar is scaled by the reference magnitude there (the same relative accuracy)
+    ms = Sk == 1
+    compare("cross O", f64(o), ro, "o")
+    compare("cross LSE", f64(lse), rl, "lse")
+    compare("cross dQ", f64(dq), rdq, "dq", ms)
+    compare("cross dK", f64(dk), rdk, "dk", ms)
+    compare("cross dV", f64(dv), rdv, "dv", ms)
+    if m is not None:
+        for b in range(B):
+            assert (f64(dk)[b, ~m[b]] == 0).all() and (f64(dv)[b, ~m[b]] == 0).all()
+
+
 def test_ulysses_padded_heads_equal_the_unsharded_path():
     """P = 4 does not divide H = 6: the head groups carry zero padding heads.
 

@@ -47,9 +47,12 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGS = {
     "uaa_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "uaa_attn_fwd_cross": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "uaa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "uaa_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P,
                           ctypes.c_size_t, _P]),
+    "uaa_attn_bwd_cross": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P,
+                                ctypes.c_size_t, _P]),
     "uaa_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
     "uaa_attn_bwd_noalloc_max_bytes": (ctypes.c_size_t, []),
     "uaa_seq_to_head": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
@@ -101,15 +104,17 @@ def _need_cuda(*ts):
             raise ValueError("uaa kernels run on CUDA tensors only (no CPU fallback)")
 
 
-def _bshd(name, t, ref=None):
+def _bshd(name, t, ref=None, same_s=True):
     if t.dim() != 4:
         raise ValueError(f"{name} must be (B, S, H, D), got {tuple(t.shape)}")
     if t.dtype != torch.bfloat16:
         raise TypeError(f"{name} must be bfloat16")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous BSHD")
-    if ref is not None and t.shape != ref.shape:
-        raise ValueError(f"{name} shape {tuple(t.shape)} differs from {tuple(ref.shape)}")
+    if ref is not None:
+        a, b = tuple(t.shape), tuple(ref.shape)
+        if (a != b) if same_s else (a[0] != b[0] or a[2:] != b[2:]):
+            raise ValueError(f"{name} shape {a} does not fit {b}")
 
 
 def normalize_key_mask(mask, B, S):
@@ -141,21 +146,30 @@ def normalize_key_mask(mask, B, S):
 
 # --------------------------------------------------------------------------- attention
 def attn_fwd(q, k, v, key_mask=None, scale=None, out=None, lse=None):
-    """``uaa_attn_fwd``: returns ``(out bf16 (B,S,H,D), lse fp32 (B,H,S))``."""
+    """``uaa_attn_fwd`` / ``uaa_attn_fwd_cross``: returns ``(out bf16 (B,Sq,H,D), lse fp32 (B,H,Sq))``.
+
+    ``k`` and ``v`` may have another sequence length ``Sk`` than ``q`` (cross-attention);
+    ``key_mask`` is then ``(B, Sk)``.
+    """
     _bshd("q", q)
-    _bshd("k", k, q)
-    _bshd("v", v, q)
+    _bshd("k", k, q, same_s=False)
+    _bshd("v", v, k)
     _need_cuda(q, k, v)
-    B, S, H, D = q.shape
-    mask = normalize_key_mask(key_mask, B, S)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    mask = normalize_key_mask(key_mask, B, Sk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    _check(lib().uaa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), B, S, H, D,
-                              float(scale), _P(_stream(q.device))))
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if Sq == Sk:
+        _check(lib().uaa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), B, Sq, H, D,
+                                  float(scale), _P(_stream(q.device))))
+    else:
+        _check(lib().uaa_attn_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), B, Sq, Sk, H,
+                                        D, float(scale), _P(_stream(q.device))))
     return out, lse
 
 
@@ -164,25 +178,38 @@ def attn_bwd_workspace_bytes(B, S, H, D) -> int:
 
 
 def attn_bwd(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=None, dv=None, workspace=None):
-    """``uaa_attn_bwd``: returns ``(dq, dk, dv)`` in bf16 BSHD."""
-    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
-        _bshd(n, t, q)
+    """``uaa_attn_bwd`` / ``uaa_attn_bwd_cross``: returns ``(dq, dk, dv)`` in bf16 BSHD.
+
+    ``k``, ``v`` (and ``dk``, ``dv``) may have another sequence length than ``q``.
+    """
+    _bshd("q", q)
+    _bshd("k", k, q, same_s=False)
+    _bshd("v", v, k)
+    _bshd("out", out, q)
+    _bshd("dout", dout, q)
     _need_cuda(q, k, v, out, dout, lse)
-    B, S, H, D = q.shape
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous():
-        raise ValueError("lse must be contiguous fp32 (B, H, S)")
-    mask = normalize_key_mask(key_mask, B, S)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 (B, H, Sq)")
+    mask = normalize_key_mask(key_mask, B, Sk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    nbytes = attn_bwd_workspace_bytes(B, S, H, D)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    nbytes = attn_bwd_workspace_bytes(B, Sq, H, D)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
-    _check(lib().uaa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask), _ptr(dq),
-                              _ptr(dk), _ptr(dv), B, S, H, D, float(scale), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _P(_stream(q.device))))
+    wsb = workspace.numel() * workspace.element_size()
+    if Sq == Sk:
+        _check(lib().uaa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Sq, H, D, float(scale), _ptr(workspace), wsb,
+                                  _P(_stream(q.device))))
+    else:
+        _check(lib().uaa_attn_bwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), B, Sq, Sk, H, D, float(scale),
+                                        _ptr(workspace), wsb, _P(_stream(q.device))))
     return dq, dk, dv
 
 

@@ -44,7 +44,7 @@
 
 namespace uaa {
 
-int validate_attn_sizes(const char* fn, int B, int S, int H, int D, float scale);
+int validate_attn_sizes(const char* fn, int B, int Sq, int Sk, int H, int D, float scale);
 int check_dev_ptr(const char* fn, const char* name, const void* p);
 
 namespace {
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const float* __restrict__ nl2, const float* __restrict__ delta,
                          const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ dk,
-                         __nv_bfloat16* __restrict__ dv, int S, int H, int num_items, float scale,
+                         __nv_bfloat16* __restrict__ dv, int Sq, int Sk, int H, int num_items, float scale,
                          float scale_log2, DevCtx ctx) {
   using L = DkdvLayout<D>;
   constexpr int kChunks = D / 64;
@@ -255,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nkt = (S + kBT - 1) / kBT;
-  const int nqt = nkt;
+  const int nkt = (Sk + kBT - 1) / kBT;  // key tiles: the work items
+  const int nqt = (Sq + kBT - 1) / kBT;  // query tiles: the inner loop
   const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nq = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      if (kMask && !key_tile_any(mask, w.b, S, w.t)) continue;
+      if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) continue;
       if (lane == 0) {
         if (it > 0) ok = wait_or_abort(&ctl->bar_kv_empty, (it - 1) & 1, ctx, ctl);
         if (ok) {
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const size_t row0 = ((size_t)w.b * H + w.h) * padded_rows(S);
+      const size_t row0 = ((size_t)w.b * H + w.h) * padded_rows(Sq);
       for (int i = 0; ok && i < nqt; ++i, ++nq) {
         const int qs = nq % L::kQStages;
         const uint32_t qu = nq / L::kQStages;
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* turn = &ctl->turn;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      if (kMask && !key_tile_any(mask, w.b, S, w.t)) continue;
+      if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) continue;
       if (lane == 0) {
         auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
         auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
@@ -476,10 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
       const int key = w.t * kBT + jrow;
-      if (kMask && !key_tile_any(mask, w.b, S, w.t)) {
+      if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) {
         // no attended key in this tile: dK = dV = 0
-        if (key < S) {
-          const size_t off = (((size_t)w.b * S + key) * H + w.h) * D + hf * (D / 2);
+        if (key < Sk) {
+          const size_t off = (((size_t)w.b * Sk + key) * H + w.h) * D + hf * (D / 2);
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             *reinterpret_cast<uint4*>(dk + off + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const bool kvalid = key < S && (!kMask || key_mask[(size_t)w.b * S + key] != 0);
+      const bool kvalid = key < Sk && (!kMask || key_mask[(size_t)w.b * Sk + key] != 0);
       for (int i = 0; i < nqt; ++i) {
         const uint32_t g = nq + i;
         const int qs = g % L::kQStages;
@@ -561,12 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_acc_done, it & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
-      const size_t off = (((size_t)w.b * S + key) * H + w.h) * D + hf * (D / 2);
+      const size_t off = (((size_t)w.b * Sk + key) * H + w.h) * D + hf * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
         tmem_ld32(tl + kColDV + hf * (D / 2) + 32 * c, gg);
-        if (key < S) {
+        if (key < Sk) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_ld32(tl + kColDK + hf * (D / 2) + 32 * c, gg);
-        if (key < S) {
+        if (key < Sk) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const float* __restrict__ nl2g, const float* __restrict__ delta,
                        const uint8_t* __restrict__ key_mask, const __nv_bfloat16* __restrict__ qg,
-                       const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int S, int H,
+                       const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int Sq, int Sk, int H,
                        int num_items, float scale, float scale_log2, DevCtx ctx) {
   using L = DqLayout<D>;
   constexpr int kChunks = D / 64;
@@ -667,8 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nkt = (S + kBT - 1) / kBT;
-  const int nqt = nkt;
+  const int nkt = (Sk + kBT - 1) / kBT;  // key tiles: the inner loop
+  const int nqt = (Sq + kBT - 1) / kBT;  // query tiles: the work items
   const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
@@ -716,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < nkt; ++j) {
         uint32_t words[4] = {0u, 0u, 0u, 0u};
         if (kMask) {
-          key_tile_bits(mask, w.b, S, j, words);
+          key_tile_bits(mask, w.b, Sk, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
 #pragma unroll
@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the key tiles of this item, in order (all lanes evaluate the same mask)
       auto next_tile = [&](int from) {
         for (int jj = from; jj < nkt; ++jj)
-          if (!kMask || key_tile_any(mask, w.b, S, jj)) return jj;
+          if (!kMask || key_tile_any(mask, w.b, Sk, jj)) return jj;
         return nkt;
       };
       int j = next_tile(0);
@@ -893,14 +893,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q = w.t * kBT + row;
       {
         // the previous item's MMAs have all completed (its dq_done was waited on)
-        const __nv_bfloat16* src = (hf == 0 ? qg : dog) + (((size_t)w.b * S + q) * H + w.h) * D;
+        const __nv_bfloat16* src = (hf == 0 ? qg : dog) + (((size_t)w.b * Sq + q) * H + w.h) * D;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           uint32_t wv[32];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (q < S) v = __ldg(reinterpret_cast<const uint4*>(src) + 8 * c + t);
+            if (q < Sq) v = __ldg(reinterpret_cast<const uint4*>(src) + 8 * c + t);
             wv[4 * t + 0] = v.x;
             wv[4 * t + 1] = v.y;
             wv[4 * t + 2] = v.z;
@@ -912,14 +912,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->bar_qdo_ready);
       }
       // rows past S read the padding (-inf, 0)
-      const size_t prow = ((size_t)w.b * H + w.h) * padded_rows(S) + q;
+      const size_t prow = ((size_t)w.b * H + w.h) * padded_rows(Sq) + q;
       const float nl2 = nl2g[prow];
       const float dl = delta[prow];
       int ntiles = 0;
       for (int j = 0; j < nkt; ++j) {
         uint32_t words[4];
         if (kMask) {
-          key_tile_bits(mask, w.b, S, j, words);
+          key_tile_bits(mask, w.b, Sk, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
         // is there a next key tile?  Its K and V are read by the MMAs this tile's
@@ -928,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool has_next = j + 1 < nkt;
         if (kMask) {
           int jn = j + 1;
-          while (jn < nkt && !key_tile_any(mask, w.b, S, jn)) ++jn;
+          while (jn < nkt && !key_tile_any(mask, w.b, Sk, jn)) ++jn;
           has_next = jn < nkt;
         }
         if (has_next) {
@@ -961,8 +961,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!((w0 >> c) & 1u)) p[c] = 0.f;
               if (!((w1 >> c) & 1u)) p[32 + c] = 0.f;
             }
-          } else if ((j + 1) * kBT > S) {
-            const int lim = S - j * kBT - 64 * hf;
+          } else if ((j + 1) * kBT > Sk) {
+            const int lim = Sk - j * kBT - 64 * hf;
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c >= lim) p[c] = 0.f;
@@ -994,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dq_done, it & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
-      __nv_bfloat16* drow = dq + (((size_t)w.b * S + q) * H + w.h) * D + hf * (D / 2);
+      __nv_bfloat16* drow = dq + (((size_t)w.b * Sq + q) * H + w.h) * D + hf * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
@@ -1003,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 32; ++t) gg[t] = 0.f;
         }
-        if (q < S) {
+        if (q < Sq) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -1065,33 +1065,36 @@ int record_prof(int i, cudaStream_t stream) {
 
 template <int D, bool kMask>
 int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
-               const uint8_t* mask, void* dq, void* dk, void* dv, int B, int S, int H, float scale, float* delta,
-               cudaStream_t stream, const DevCtx& ctx) {
-  const size_t rows = (size_t)B * S * H;
-  float* nl2 = delta + (size_t)B * H * padded_rows(S);
+               const uint8_t* mask, void* dq, void* dk, void* dv, int B, int Sq, int Sk, int H, float scale,
+               float* delta, cudaStream_t stream, const DevCtx& ctx) {
+  const size_t rows = (size_t)B * Sq * H;
+  float* nl2 = delta + (size_t)B * H * padded_rows(Sq);
   bwd_preprocess_kernel<D><<<grid_cap(rows * 8, 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, nl2, B, S,
-      padded_rows(S), H);
+      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, nl2, B, Sq,
+      padded_rows(Sq), H);
   int st = check_launch("uaa_attn_bwd (preprocess)");
   if (st) return st;
   CUtensorMap mq, mk, mv, mdo;
-  if ((st = encode_bshd_map(&mq, q, B, S, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mk, k, B, S, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mv, v, B, S, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mdo, dout, B, S, H, D, 128))) return st;
-  const long long ntiles = (S + kBT - 1) / kBT;
-  const long long items = ntiles * H * B;
-  if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_bwd: too many work items");
-  const int grid = (int)(items < sm_count() ? items : sm_count());
+  if ((st = encode_bshd_map(&mq, q, B, Sq, H, D, 128))) return st;
+  if ((st = encode_bshd_map(&mk, k, B, Sk, H, D, 128))) return st;
+  if ((st = encode_bshd_map(&mv, v, B, Sk, H, D, 128))) return st;
+  if ((st = encode_bshd_map(&mdo, dout, B, Sq, H, D, 128))) return st;
+  // dK/dV items are key tiles, dQ items are query tiles
+  const long long items_k = (long long)((Sk + kBT - 1) / kBT) * H * B;
+  const long long items_q = (long long)((Sq + kBT - 1) / kBT) * H * B;
+  if (items_k > INT32_MAX || items_q > INT32_MAX)
+    return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_bwd: too many work items");
+  const int grid_k = (int)(items_k < sm_count() ? items_k : sm_count());
+  const int grid_q = (int)(items_q < sm_count() ? items_q : sm_count());
   if ((st = record_prof(0, stream))) return st;
   {
     auto kern = attn_bwd_dkdv_kernel<D, kMask>;
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
-                                           static_cast<__nv_bfloat16*>(dv), S, H, (int)items, scale,
-                                           scale * kLog2e, ctx);
+    kern<<<grid_k, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
+                                             static_cast<__nv_bfloat16*>(dv), Sq, Sk, H, (int)items_k, scale,
+                                             scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
   }
   if ((st = record_prof(1, stream))) return st;
@@ -1100,9 +1103,9 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DqLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<const __nv_bfloat16*>(q),
-                                           static_cast<const __nv_bfloat16*>(dout), static_cast<__nv_bfloat16*>(dq),
-                                           S, H, (int)items, scale, scale * kLog2e, ctx);
+    kern<<<grid_q, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<const __nv_bfloat16*>(q),
+                                             static_cast<const __nv_bfloat16*>(dout), static_cast<__nv_bfloat16*>(dq),
+                                             Sq, Sk, H, (int)items_q, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dQ)"))) return st;
   }
   return record_prof(2, stream);
@@ -1125,14 +1128,15 @@ extern "C" size_t uaa_attn_bwd_workspace_bytes(int B, int S, int H, int D) {
   return (((size_t)B * H * padded_rows(S) * 8) + 255) & ~(size_t)255;
 }
 
-extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
-                            const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int B, int S,
-                            int H, int D, float scale, void* workspace, size_t workspace_bytes,
-                            uaa_stream_t stream) {
+extern "C" int uaa_attn_bwd_cross(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                  const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int B,
+                                  int Sq, int Sk, int H, int D, float scale, void* workspace, size_t workspace_bytes,
+                                  uaa_stream_t stream) {
   const char* fn = "uaa_attn_bwd";
-  int st = validate_attn_sizes(fn, B, S, H, D, scale);
+  int st = validate_attn_sizes(fn, B, Sq, Sk, H, D, scale);
   if (st) return st;
-  if ((uint64_t)B * S * H == 0) return UAA_OK;
+  if ((uint64_t)B * H == 0 || (uint64_t)Sq + Sk == 0) return UAA_OK;
+  if (Sq == 0) return set_error(UAA_ERR_INVALID_ARG, "%s: keys without queries (Sq = 0)", fn);
   if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
       (st = check_dev_ptr(fn, "out", out)) || (st = check_dev_ptr(fn, "dout", dout)) ||
       (st = check_dev_ptr(fn, "dq", dq)) || (st = check_dev_ptr(fn, "dk", dk)) || (st = check_dev_ptr(fn, "dv", dv)))
@@ -1141,7 +1145,7 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
     return set_error(UAA_ERR_INVALID_ARG, "%s: lse is NULL or not 4-byte aligned", fn);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return set_error(UAA_ERR_INVALID_ARG, "%s: workspace is NULL or not 256-byte aligned", fn);
-  const size_t need = uaa_attn_bwd_workspace_bytes(B, S, H, D);
+  const size_t need = uaa_attn_bwd_workspace_bytes(B, Sq, H, D);
   if (workspace_bytes < need)
     return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
   DevCtx ctx;
@@ -1149,14 +1153,22 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
   float* delta = static_cast<float*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64)
-    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
-                                           ctx)
-                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
-                                            ctx);
-  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
-                                          ctx)
-                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, H, scale, delta, s,
-                                           ctx);
+    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale, delta,
+                                           s, ctx)
+                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale,
+                                            delta, s, ctx);
+  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale, delta,
+                                          s, ctx)
+                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale, delta,
+                                           s, ctx);
+}
+
+extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                            const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int B, int S,
+                            int H, int D, float scale, void* workspace, size_t workspace_bytes,
+                            uaa_stream_t stream) {
+  return uaa_attn_bwd_cross(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, S, H, D, scale, workspace,
+                            workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1214,7 +1226,7 @@ extern "C" int uaa_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                                     const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int B,
                                     int S, int H, int D, float scale, uaa_stream_t stream) {
   const char* fn = "uaa_attn_bwd_noalloc";
-  int st = validate_attn_sizes(fn, B, S, H, D, scale);
+  int st = validate_attn_sizes(fn, B, S, S, H, D, scale);
   if (st) return st;
   if ((uint64_t)B * S * H == 0) return UAA_OK;
   const size_t need = uaa_attn_bwd_workspace_bytes(B, S, H, D);

@@ -128,7 +128,7 @@ template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const uint8_t* __restrict__ key_mask,
-                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int S, int H, int num_items,
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int Sq, int Sk, int H, int num_items,
                     float scale_log2, DevCtx ctx) {
   using L = FwdLayout<D>;
   constexpr int kChunks = D / 64;
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nqp = (S + 2 * kBM - 1) / (2 * kBM);
-  const int nkt = (S + kBN - 1) / kBN;
+  const int nqp = (Sq + 2 * kBM - 1) / (2 * kBM);
+  const int nkt = (Sk + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->bar_q_full, 1);
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const int key = j * kBN + 32 * t + lane;
-              const bool valid = key < S && key_mask[(size_t)w.b * S + key] != 0;
+              const bool valid = key < Sk && key_mask[(size_t)w.b * Sk + key] != 0;
               words[t] = __ballot_sync(0xffffffffu, valid);
             }
             if (lane == 0) {
@@ -362,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
-        } else if ((j + 1) * kBN > S) {
-          const int lim = S - j * kBN;
+        } else if ((j + 1) * kBN > Sk) {
+          const int lim = Sk - j * kBN;
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             if (c >= lim) s[c] = -INFINITY;
@@ -425,12 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int q = w.qp * 2 * kBM + t * kBM + row;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = out + (((size_t)w.b * S + q) * H + w.h) * D;
+      __nv_bfloat16* orow = out + (((size_t)w.b * Sq + q) * H + w.h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         tmem_ld32(tl + colO + 32 * c, o);
-        if (q < S) {
+        if (q < Sq) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 v;
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&ctl->bar_o_free);
-      if (q < S) lse[((size_t)w.b * H + w.h) * S + q] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
+      if (q < Sq) lse[((size_t)w.b * H + w.h) * Sq + q] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
       g += nkt;
     }
   }
@@ -483,33 +483,36 @@ int sm_count() {
 
 template <int D, bool kMask>
 int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, void* out, float* lse, int B,
-               int S, int H, float scale, cudaStream_t stream, const DevCtx& ctx) {
+               int Sq, int Sk, int H, float scale, cudaStream_t stream, const DevCtx& ctx) {
   CUtensorMap mq, mk, mv;
   int st;
-  if ((st = encode_bshd_map(&mq, q, B, S, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mk, k, B, S, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mv, v, B, S, H, D, 128))) return st;
+  if ((st = encode_bshd_map(&mq, q, B, Sq, H, D, 128))) return st;
+  if ((st = encode_bshd_map(&mk, k, B, Sk, H, D, 128))) return st;
+  if ((st = encode_bshd_map(&mv, v, B, Sk, H, D, 128))) return st;
   auto kern = attn_fwd_kernel<D, kMask>;
   const int smem = FwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_fwd: smem attribute: %s", cudaGetErrorString(e));
-  const long long nqp = (S + 2 * kBM - 1) / (2 * kBM);
+  const long long nqp = (Sq + 2 * kBM - 1) / (2 * kBM);
   const long long items = nqp * H * B;
   if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_fwd: too many work items");
   const int grid = (int)(items < sm_count() ? items : sm_count());
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mask, static_cast<__nv_bfloat16*>(out), lse, S, H, (int)items,
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mask, static_cast<__nv_bfloat16*>(out), lse, Sq, Sk, H, (int)items,
                                          scale * kLog2e, ctx);
   return check_launch("uaa_attn_fwd");
 }
 
 }  // namespace
 
-int validate_attn_sizes(const char* fn, int B, int S, int H, int D, float scale) {
-  if (B < 0 || S < 0 || H < 0) return set_error(UAA_ERR_INVALID_ARG, "%s: negative size B=%d S=%d H=%d", fn, B, S, H);
+int validate_attn_sizes(const char* fn, int B, int Sq, int Sk, int H, int D, float scale) {
+  if (B < 0 || Sq < 0 || Sk < 0 || H < 0)
+    return set_error(UAA_ERR_INVALID_ARG, "%s: negative size B=%d Sq=%d Sk=%d H=%d", fn, B, Sq, Sk, H);
+  if (Sq > 0 && Sk == 0) return set_error(UAA_ERR_INVALID_ARG, "%s: queries without keys (Sk = 0)", fn);
   if (D != 64 && D != 128) return set_error(UAA_ERR_UNSUPPORTED, "%s: D=%d (only 64 and 128 are built)", fn, D);
   if (!(scale > 0.f) || !isfinite(scale))
     return set_error(UAA_ERR_INVALID_ARG, "%s: scale must be positive and finite", fn);
   if (B > 65535 || H > 65535) return set_error(UAA_ERR_UNSUPPORTED, "%s: B and H must be <= 65535", fn);
+  const uint64_t S = (uint64_t)(Sq > Sk ? Sq : Sk);
   if ((uint64_t)B * S * H * D * 4 >= (1ull << 40))
     return set_error(UAA_ERR_UNSUPPORTED, "%s: tensor larger than the TMA stride range", fn);
   return UAA_OK;
@@ -526,12 +529,12 @@ int check_dev_ptr(const char* fn, const char* name, const void* p) {
 
 using namespace uaa;
 
-extern "C" int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
-                            float* lse, int B, int S, int H, int D, float scale, uaa_stream_t stream) {
+extern "C" int uaa_attn_fwd_cross(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
+                                  float* lse, int B, int Sq, int Sk, int H, int D, float scale, uaa_stream_t stream) {
   const char* fn = "uaa_attn_fwd";
-  int st = validate_attn_sizes(fn, B, S, H, D, scale);
+  int st = validate_attn_sizes(fn, B, Sq, Sk, H, D, scale);
   if (st) return st;
-  if ((uint64_t)B * S * H == 0) return UAA_OK;
+  if ((uint64_t)B * Sq * H == 0) return UAA_OK;
   if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
       (st = check_dev_ptr(fn, "out", out)))
     return st;
@@ -541,8 +544,13 @@ extern "C" int uaa_attn_fwd(const void* q, const void* k, const void* v, const u
   if ((st = get_dev_ctx(&ctx))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64)
-    return key_mask ? launch_fwd<64, true>(q, k, v, key_mask, out, lse, B, S, H, scale, s, ctx)
-                    : launch_fwd<64, false>(q, k, v, key_mask, out, lse, B, S, H, scale, s, ctx);
-  return key_mask ? launch_fwd<128, true>(q, k, v, key_mask, out, lse, B, S, H, scale, s, ctx)
-                  : launch_fwd<128, false>(q, k, v, key_mask, out, lse, B, S, H, scale, s, ctx);
+    return key_mask ? launch_fwd<64, true>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx)
+                    : launch_fwd<64, false>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx);
+  return key_mask ? launch_fwd<128, true>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx)
+                  : launch_fwd<128, false>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx);
+}
+
+extern "C" int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
+                            float* lse, int B, int S, int H, int D, float scale, uaa_stream_t stream) {
+  return uaa_attn_fwd_cross(q, k, v, key_mask, out, lse, B, S, S, H, D, scale, stream);
 }
