@@ -225,7 +225,6 @@ struct DkdvCtl {
   uint64_t bar_acc_done, bar_acc_free, bar_final[2];
   uint32_t tmem_base;
   int abort;
-  uint32_t turn;  // MMA-issue token: bursts released so far
 };
 static_assert(sizeof(DkdvCtl) <= 256, "control block");
 
@@ -273,14 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->bar_s_full, 1);
     mbar_init(&ctl->bar_dp_full, 1);
-    mbar_init(&ctl->bar_p_ready, kComputeThreads);
-    mbar_init(&ctl->bar_ds_ready, kComputeThreads);
+    // the compute warps plus the other issuer's hand-over (see the issuers)
+    mbar_init(&ctl->bar_p_ready, kComputeThreads + 1);
+    mbar_init(&ctl->bar_ds_ready, kComputeThreads + 1);
     mbar_init(&ctl->bar_acc_done, 2);
     mbar_init(&ctl->bar_acc_free, kComputeThreads);
     mbar_init(&ctl->bar_final[0], 1);
     mbar_init(&ctl->bar_final[1], 1);
     ctl->abort = 0;
-    ctl->turn = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -361,44 +360,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // thread:
     //   warp 9  (chain v): S^T_0 | dV_0 S^T_1 | dV_1 S^T_2 | ...   (after p_ready)
     //   warp 10 (chain k): dP^T_0 | dK_0 dP^T_1 | dK_1 dP^T_2 | ... (after ds_ready)
-    // The two threads take turns burst by burst (a token in shared memory), so
-    // the tensor pipe runs v, k, v, k, ... and each thread does its barrier
-    // waits while the other's burst runs; the token is handed over four MMAs
-    // before the end of a burst.  The tensor pipe queues only about one MMA,
-    // and a single issuing thread that stopped to wait between GEMMs would leave
-    // it idle for a few hundred cycles per wait.  Within a chain the MMAs of one
+    // The two threads take turns burst by burst, so the tensor pipe runs v, k,
+    // v, k, ... and each thread waits while the other's burst runs.  The turn
+    // is handed over through the handshake barriers themselves: chain k arrives
+    // on p_ready(i) once it has issued all but four MMAs of the burst holding
+    // dP^T_i, chain v on ds_ready(i) once it has done so for the burst holding
+    // dV_i, so each thread's one wait per burst covers both the compute warps'
+    // handshake and its turn.  The tensor pipe queues only about one MMA, and a
+    // single issuing thread that stopped to wait between GEMMs would leave it
+    // idle for a few hundred cycles per wait.  Within a chain the MMAs of one
     // thread execute in order: dV_i reads P^T_i before S^T_{i+1} overwrites
     // those columns, and dK_i reads dS^T_i before dP^T_{i+1} does.
     const int c = warp - kMmaWarp;  // 0: chain v, 1: chain k
     bool ok = true;
     uint32_t nq = 0, it = 0;
-    uint32_t m = 0;  // bursts of this thread so far; its burst m has turn 2m + c
     const uint32_t sK = sbase + L::kK;
     const uint32_t sV = sbase + L::kV;
-    volatile uint32_t* turn = &ctl->turn;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
       if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) continue;
       if (lane == 0) {
         auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
         auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
-        auto take_turn = [&]() -> bool {
-          const uint32_t want = 2 * m + (uint32_t)c;
-          if (*turn >= want) return true;
-          const uint64_t t0 = globaltimer_ns();
-          while (*turn < want) {
-            if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-            if (globaltimer_ns() - t0 > ctx.timeout_ns) {
-              atomicOr(ctx.status, kStatusTimeout);
-              *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-              return false;
-            }
-          }
-          return true;
-        };
-        auto pass_turn = [&]() { *turn = 2 * m + (uint32_t)c + 1; };
+        // hand the turn to the other chain (see above)
+        auto pass_turn = [&]() { mbar_arrive(c == 0 ? &ctl->bar_ds_ready : &ctl->bar_p_ready); };
         // the first GEMM of a chain for query tile g: S^T_g = K Q_g^T or dP^T_g = V dO_g^T;
-        // hands the token over when `pass` after its first D/16 - 4 MMAs
+        // hands the turn over when `pass` four MMAs before its end (after its first MMA for D = 64)
         auto issue_first = [&](uint32_t g, bool pass) {
           const uint64_t a0 = sdesc_sw128(c == 0 ? sK : sV, 16, 1024);
           const uint64_t b0 = sdesc_sw128(c == 0 ? sq(g) : sdo(g), 16, 1024);
@@ -431,11 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = c == 0 ? wait_or_abort(&ctl->bar_q_full[nq % L::kQStages], (nq / L::kQStages) & 1, ctx, ctl)
                       : wait_or_abort(&ctl->bar_do_full[nq % L::kDStages], (nq / L::kDStages) & 1, ctx, ctl);
         }
-        if (ok) ok = take_turn();
         if (ok) {
           tc_fence_after();
-          issue_first(nq, true);
-          ++m;
+          // chain k's first burst (dP^T of the item's first tile) releases chain v's first dV burst
+          issue_first(nq, c == 1);
           mma_issued = true;
         }
         // Inside the query loop the compute warps arrive on p_ready / ds_ready only
@@ -447,18 +433,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the previous item's epilogue must have read dK / dV
             if (!(ok = wait_or_abort(&ctl->bar_acc_free, (it - 1) & 1, ctx, ctl))) break;
           }
-          if (!(ok = take_turn())) break;
           tc_fence_after();
           const bool more = i + 1 < nqt;
-          issue_acc(g, i == 0, !more);
+          // chain v's burst (dV_i, S^T_{i+1}) releases dK_i; chain k's (dK_i, dP^T_{i+1}) releases dV_{i+1}
+          issue_acc(g, i == 0, c == 0 && !more);
           if (more) issue_first(g + 1, true);
-          ++m;
         }
         if (ok) {
           mma_commit(&ctl->bar_acc_done);
           mma_commit(&ctl->bar_kv_empty);
         } else {
-          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer may be waiting for our turn
+          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer waits for our hand-over
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -638,7 +623,6 @@ struct DqCtl {
   uint64_t bar_dq_done, bar_dq_free, bar_final[2];
   uint32_t tmem_base;
   int abort;
-  uint32_t turn;  // MMA-issue token: bursts released so far
 };
 static_assert(sizeof(DqCtl) <= 512, "control block");
 
@@ -678,15 +662,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->bar_kv_empty[s], 2);  // one release per issuer
     }
     mbar_init(&ctl->bar_s_full, 1);
-    mbar_init(&ctl->bar_s_read, kComputeThreads);
+    // the compute warps plus the other issuer's hand-over (see the issuers)
+    mbar_init(&ctl->bar_s_read, kComputeThreads + 1);
     mbar_init(&ctl->bar_dp_full, 1);
-    mbar_init(&ctl->bar_ds_ready, kComputeThreads);
+    mbar_init(&ctl->bar_ds_ready, kComputeThreads + 1);
     mbar_init(&ctl->bar_dq_done, 1);
     mbar_init(&ctl->bar_dq_free, kComputeThreads);
     mbar_init(&ctl->bar_final[0], 1);
     mbar_init(&ctl->bar_final[1], 1);
     ctl->abort = 0;
-    ctl->turn = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -743,35 +727,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two chains, each issued by its own thread, per processed key tile g:
     //   warp 9  (chain s): S_0 | S_1 | S_2 | ...            (S_{g+1} after s_read(g))
     //   warp 10 (chain d): dP_0 | dQ_0 dP_1 | dQ_1 dP_2 | ... (after ds_ready(g))
-    // The threads take turns burst by burst (a token in shared memory; chain s
-    // passes an empty burst after the last tile so both have the same count),
-    // so each waits for its handshake while the other's burst runs; the token
-    // is handed over four MMAs before the end of a burst.  The tensor pipe
-    // queues only about one MMA, and a single issuing thread that stopped to
-    // wait between GEMMs would leave it idle for a few hundred cycles per wait.
-    // In chain d, dQ_g reads dS_g (in the dP columns) before dP_{g+1}
-    // overwrites them: the MMAs of one thread execute in order.
+    // The threads take turns burst by burst, each waiting while the other's
+    // burst runs.  The turn is handed over through the handshake barriers
+    // themselves: chain d arrives on s_read(g) once it has issued all but four
+    // MMAs of the burst holding dP_g, chain s on ds_ready(g) once it has done so
+    // for S_{g+1} (after the last key tile, once s_read(last) has completed), so
+    // each thread's one wait per burst covers both the compute warps' handshake
+    // and its turn.  The tensor pipe queues only about one MMA, and a single
+    // issuing thread that stopped to wait between GEMMs would leave it idle for
+    // a few hundred cycles per wait.  In chain d, dQ_g reads dS_g (in the dP
+    // columns) before dP_{g+1} overwrites them: the MMAs of one thread execute
+    // in order.
     const int c = warp - kMmaWarp;  // 0: chain s, 1: chain d
     bool ok = true;
     uint32_t g = 0, it = 0;  // g: processed key tiles across items
-    uint32_t m = 0;          // bursts of this thread so far; its burst m has turn 2m + c
-    volatile uint32_t* turn = &ctl->turn;
     auto ring = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
-    auto take_turn = [&]() -> bool {
-      const uint32_t want = 2 * m + (uint32_t)c;
-      if (*turn >= want) return true;
-      const uint64_t t0 = globaltimer_ns();
-      while (*turn < want) {
-        if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-        if (globaltimer_ns() - t0 > ctx.timeout_ns) {
-          atomicOr(ctx.status, kStatusTimeout);
-          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-          return false;
-        }
-      }
-      return true;
-    };
-    auto pass_turn = [&]() { *turn = 2 * m + (uint32_t)c + 1; };
+    // hand the turn to the other chain (see above)
+    auto pass_turn = [&]() { mbar_arrive(c == 0 ? &ctl->bar_ds_ready : &ctl->bar_s_read); };
     // S_gg = Q K^T (A = Q in TMEM); releases (this thread's share of) the slots of K_gg and V_gg
     auto issue_s = [&](uint32_t gg, bool pass) {
       const uint32_t nk = 2 * gg;
@@ -835,12 +807,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t n0 = 2 * g + (uint32_t)c;  // K_g for chain s, V_g for chain d
           ok = wait_or_abort(&ctl->bar_kv_full[n0 % R], (n0 / R) & 1, ctx, ctl);
         }
-        if (ok) ok = take_turn();
         if (ok) {
           tc_fence_after();
-          if (c == 0) issue_s(g, true);
+          // chain d's first burst (dP of the item's first key tile) releases chain s's S of the next tile
+          if (c == 0) issue_s(g, false);
           else issue_dp(g, true);
-          ++m;
           mma_issued = true;
         }
       }
@@ -850,25 +821,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jn = next_tile(j + 1);
         if (lane == 0) {
           if (c == 0) {
-            // S of the next key tile once this one's S was read into registers
-            if (jn < nkt) ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
-            if (ok) ok = take_turn();
+            // S of the next key tile once this one's S was read into registers (after the
+            // last tile: only the hand-over, which must follow s_read of that tile)
+            ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
             if (ok) {
               tc_fence_after();
               if (jn < nkt) issue_s(g + 1, true);
-              else pass_turn();  // empty burst: keeps the two threads' burst counts equal
+              else pass_turn();
             }
           } else {
             ok = wait_or_abort(&ctl->bar_ds_ready, g & 1, ctx, ctl);
             if (ok && first && it > 0) ok = wait_or_abort(&ctl->bar_dq_free, (it - 1) & 1, ctx, ctl);
-            if (ok) ok = take_turn();
             if (ok) {
               tc_fence_after();
-              issue_dq(g, first, jn >= nkt);
+              issue_dq(g, first, false);
               if (jn < nkt) issue_dp(g + 1, true);
             }
           }
-          ++m;
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         first = false;
@@ -879,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && c == 1) mma_commit(&ctl->bar_dq_done);
       __syncwarp();
     }
-    if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer may wait for our turn
+    if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer waits for our hand-over
   } else {
     // ------------------------------------------------------------ compute warps 0..7
     const int qd = warp & 3;
