@@ -14,11 +14,15 @@
 //              128 keys through a 5-stage ring (128-byte swizzled, 64 columns
 //              per box); with a mask it also packs each tile's 128 mask bits
 //              into shared memory.
-//   warp 9     tcgen05 issuer (one thread), ping-pong over the two tiles:
+//   warp 9     tcgen05 issuer (lane 0), ping-pong over the two tiles:
 //                S0_0 S1_0 | PV0_0 S0_1 | PV1_0 S1_1 | PV0_1 S0_2 | ...
 //              so while one softmax warpgroup works on its tile the tensor
 //              core runs the other tile's MMAs.  PV reads P from TMEM (A
-//              operand in tensor memory) and V from shared memory.
+//              operand in tensor memory) and V from shared memory.  The
+//              softmax warpgroups hand P over through hardware named
+//              barriers, not mbarriers: a load by the issuing thread waits
+//              behind the MMAs it has queued, which would drain the tensor
+//              pipe at every hand-over.
 //   warps 0-3  softmax of query tile 0, warps 4-7 softmax of tile 1: thread r
 //              owns query row r (TMEM lane r), so the row max and row sum are
 //              thread-local; online softmax in base 2 with a lazily updated
@@ -44,7 +48,11 @@ constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes (one swizzle col
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;
+// named barrier kBarP + t: "P_t is in TMEM" (the 128 threads of softmax warpgroup t
+// arrive, the issuer warp syncs)
+constexpr uint32_t kBarP = 1;
+constexpr uint32_t kBarPCount = 128 + 32;  // log2 units: rescale O only when the max grows by > 2^8
 
 template <int D>
 struct FwdLayout {
@@ -64,7 +72,6 @@ struct FwdCtl {
   uint64_t bar_kv_full[5];
   uint64_t bar_kv_empty[5];
   uint64_t bar_s_full[2];
-  uint64_t bar_p_full[2];
   uint64_t bar_pv_done[2];
   uint64_t bar_o_free;
   uint64_t bar_final;
@@ -160,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&ctl->bar_s_full[w], 1);
-      mbar_init(&ctl->bar_p_full[w], 128);
       mbar_init(&ctl->bar_pv_done[w], 1);
     }
     mbar_init(&ctl->bar_o_free, 256);
@@ -245,81 +251,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = true;
-      uint32_t g = 0;  // global tile counter across items (phase index of s/p/pv barriers)
-      uint32_t it = 0;
-      auto ring_addr = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
-      auto issue_s = [&](int t, uint32_t nk, uint32_t gg) {
-        const uint32_t sQ = sbase + L::kQ + t * L::kTileBytes;
-        const uint32_t sK = ring_addr(nk);
-        const uint32_t d = tmem + (uint32_t)(t * kBN);
-        const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dk0 = sdesc_sw128(sK, 16, 1024);
+    // The whole warp runs the schedule (named barriers take whole warps); lane 0
+    // issues.  Within an item this warp executes no memory instruction: it learns
+    // that P_t is in TMEM from named barrier kBarP + t, which the softmax
+    // warpgroup of tile t arrives on.
+    const bool leader = lane == 0;
+    bool ok = true;
+    uint32_t g = 0;  // global tile counter across items (phase index of s/pv barriers)
+    uint32_t it = 0;
+    auto ring_addr = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
+    auto issue_s = [&](int t, uint32_t nk) {
+      const uint32_t sQ = sbase + L::kQ + t * L::kTileBytes;
+      const uint32_t sK = ring_addr(nk);
+      const uint32_t d = tmem + (uint32_t)(t * kBN);
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024), dk0 = sdesc_sw128(sK, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16(d, desc_add(dq0, off), desc_add(dk0, off), kIdescS, kk > 0);
-        }
-        mma_commit(&ctl->bar_s_full[t]);
-        (void)gg;
-      };
-      auto issue_pv = [&](int t, uint32_t nv, bool acc) {
-        const uint32_t aP = tmem + (uint32_t)(t * kBN);  // P_t: 128 rows x 128 keys bf16 = 64 columns
-        const uint32_t sV = ring_addr(nv);
-        const uint32_t d = tmem + 256 + (uint32_t)(t * D);
-        const uint64_t dv0 = sdesc_sw128(sV, kChunkBytes, 1024);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+        mma_bf16(d, desc_add(dq0, off), desc_add(dk0, off), kIdescS, kk > 0);
+      }
+      mma_commit(&ctl->bar_s_full[t]);
+    };
+    auto issue_pv = [&](int t, uint32_t nv, bool acc) {
+      const uint32_t aP = tmem + (uint32_t)(t * kBN);  // P_t: 128 rows x 128 keys bf16 = 64 columns
+      const uint32_t sV = ring_addr(nv);
+      const uint32_t d = tmem + 256 + (uint32_t)(t * D);
+      const uint64_t dv0 = sdesc_sw128(sV, kChunkBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(d, aP + kk * 8, desc_add(dv0, kk * 2048), kIdescPV,
-                      (acc || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->bar_pv_done[t]);
-      };
-      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
-        if (!(ok = wait_or_abort(&ctl->bar_q_full, it & 1, ctx, ctl))) break;
-        tc_fence_after();
-        // K_0 of this item: ring index 2g
-        uint32_t nk = 2 * g;
-        if (!(ok = wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl))) break;
-        tc_fence_after();
-        issue_s(0, nk, g);
-        issue_s(1, nk, g);
-        mma_commit(&ctl->bar_kv_empty[nk % R]);
-        mma_issued = true;
-        for (int j = 0; j < nkt; ++j) {
-          const uint32_t gj = g + j;
-          const uint32_t nv = 2 * gj + 1;
-          // tile 0: PV0_j, then S0_{j+1}.  The softmax warpgroups arrive on
-          // p_full only after they have seen V_j and K_{j+1} land, so this thread
-          // waits on nothing else inside the loop: each wait of the issuing
-          // thread costs the tensor pipe a few hundred cycles (it queues only
-          // about one MMA).
-          if (!(ok = wait_or_abort(&ctl->bar_p_full[0], gj & 1, ctx, ctl))) break;
-          tc_fence_after();
-          if (j == 0 && it > 0) {
-            // the previous item's epilogue must have read O before it is overwritten
-            if (!(ok = wait_or_abort(&ctl->bar_o_free, (it - 1) & 1, ctx, ctl))) break;
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_bf16_ts(d, aP + kk * 8, desc_add(dv0, kk * 2048), kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      mma_commit(&ctl->bar_pv_done[t]);
+    };
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++it) {
+      // After a failure anywhere in the CTA this warp stops issuing but still
+      // meets the softmax warpgroups at every named barrier of the schedule.
+      if (ok && *reinterpret_cast<volatile int*>(&ctl->abort)) ok = false;
+      const uint32_t nk = 2 * g;  // K_0 of this item
+      if (ok) {
+        bool w = true;
+        if (leader) {
+          w = wait_or_abort(&ctl->bar_q_full, it & 1, ctx, ctl);
+          if (w) w = wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl);
+          if (w) {
             tc_fence_after();
+            issue_s(0, nk);
+            issue_s(1, nk);
+            mma_commit(&ctl->bar_kv_empty[nk % R]);
+            mma_issued = true;
           }
+        }
+        ok = __shfl_sync(0xffffffffu, w, 0);
+      }
+      for (int j = 0; j < nkt; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t nv = 2 * gj + 1;
+        const bool more = j + 1 < nkt;
+        const uint32_t nk1 = 2 * (gj + 1);
+        // tile 0: PV0_j, then S0_{j+1}.  V_j and K_{j+1} have landed: the softmax
+        // warpgroups wait for them before they arrive.
+        named_sync(kBarP + 0, kBarPCount);
+        if (ok && j == 0 && it > 0) {
+          // the previous item's epilogue must have read O before PV0_0 overwrites it
+          bool w = true;
+          if (leader) w = wait_or_abort(&ctl->bar_o_free, (it - 1) & 1, ctx, ctl);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+        }
+        if (ok && leader) {
+          tc_fence_after();
           issue_pv(0, nv, j > 0);
-          const bool more = j + 1 < nkt;
-          const uint32_t nk1 = 2 * (gj + 1);
-          if (more) issue_s(0, nk1, gj + 1);
-          // tile 1: PV1_j, then S1_{j+1}
-          if (!(ok = wait_or_abort(&ctl->bar_p_full[1], gj & 1, ctx, ctl))) break;
+          if (more) issue_s(0, nk1);
+        }
+        __syncwarp();
+        // tile 1: PV1_j, then S1_{j+1}
+        named_sync(kBarP + 1, kBarPCount);
+        if (ok && leader) {
           tc_fence_after();
           issue_pv(1, nv, j > 0);
           mma_commit(&ctl->bar_kv_empty[nv % R]);
           if (more) {
-            issue_s(1, nk1, gj + 1);
+            issue_s(1, nk1);
             mma_commit(&ctl->bar_kv_empty[nk1 % R]);
           }
         }
-        if (!ok) break;
-        mma_commit(&ctl->bar_q_empty);  // both Q tiles are free once this item's MMAs are done
-        g += nkt;
+        __syncwarp();
       }
+      // both Q tiles are free once this item's MMAs are done
+      if (ok && leader) mma_commit(&ctl->bar_q_empty);
+      __syncwarp();
+      g += nkt;
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;                 // query tile of this warpgroup
@@ -330,24 +350,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t g = 0;
     uint32_t it = 0;
-    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++it) {
       const Item w = decode_item(item, nqp, H);
       float mu = -INFINITY;  // log2-domain offset in use (scaled max, possibly stale by < 2^8)
       float l_run = 0.f;
       for (int j = 0; j < nkt; ++j) {
         const uint32_t gj = g + j;
-        {
-          // V_j and K_{j+1}, read by the MMAs that this step's p_full releases,
+        if (ok) {
+          // V_j and K_{j+1}, read by the MMAs that this step's arrival releases,
           // have normally landed long before S_j completes: waiting here keeps
           // these waits off both the issuing thread and the S -> P path
           const uint32_t nv = 2 * gj + 1, nk1 = nv + 1;
           bool okw = wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl);
           if (okw && j + 1 < nkt) okw = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl);
+          if (okw) okw = wait_or_abort(&ctl->bar_s_full[t], gj & 1, ctx, ctl);
           ok = __all_sync(0xffffffffu, okw);
-          if (!ok) break;
         }
-        ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_s_full[t], gj & 1, ctx, ctl));
-        if (!ok) break;
+        if (!ok) {
+          // after a failure: keep meeting the issuer at every step of the schedule;
+          // a rendezvous, so this warp never runs a phase ahead of it
+          named_sync(kBarP + t, kBarPCount);
+          continue;
+        }
         tc_fence_after();
         float s[kBN];
         tmem_ld32x2(tl + colS, tl + colS + 32, *reinterpret_cast<float(*)[64]>(&s[0]));
@@ -417,11 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&ctl->bar_p_full[t]);
+        named_arrive(kBarP + t, kBarPCount);
       }
-      if (!ok) break;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (g + nkt - 1) & 1, ctx, ctl));
-      if (!ok) break;
+      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (g + nkt - 1) & 1, ctx, ctl));
+      if (!ok) {
+        g += nkt;
+        continue;
+      }
       tc_fence_after();
       const int q = w.qp * 2 * kBM + t * kBM + row;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;

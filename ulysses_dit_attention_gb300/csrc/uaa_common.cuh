@@ -139,6 +139,22 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- named barriers
+// Hardware CTA barriers 1..15 (0 is __syncthreads).  Whole, converged warps
+// take part; `count` is the number of threads (a multiple of 32) per phase.
+// The thread that issues tensor-core MMAs synchronises through these rather
+// than through an mbarrier: any load it executes (an mbarrier test included)
+// is held behind the MMAs it has queued, and the tensor pipe runs dry while
+// it waits.  bar.arrive releases and bar.sync acquires, so tcgen05 work fenced
+// with tcgen05.fence::before_thread_sync before the arrive is visible to
+// tcgen05 work issued after tcgen05.fence::after_thread_sync behind the sync.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation: warp-wide; writes the allocated base address to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
