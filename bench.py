@@ -43,9 +43,10 @@ from ulysses_dit_attention_gb300 import synth  # noqa: E402
 WORKLOAD = "ulysses_p4_n27280_h40_d128"
 
 # DRAM bytes (read + write) per attn_bwd_dkdv_kernel launch (all four 10-head groups of the workload
-# above), from the one-pass ncu capture summarised in profiles/, keyed by the SHA-256 prefix of the
-# attn_bwd.cu it was taken on; the bench reports null once the kernel source has changed since.
-DKDV_TRAFFIC = {"588b85e19c93e957": 1133441024 + 533295104}
+# above): the ncu capture of the same launch at 2 heads per group (profiles/), scaled by the five
+# times as many work items; keyed by the SHA-256 prefix of the attn_bwd.cu it was taken on, so the
+# bench reports null once the kernel source has changed since.
+DKDV_TRAFFIC = {"6daa563282562362": 5 * (226331648 + 83543296)}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
