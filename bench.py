@@ -252,6 +252,12 @@ def run_gpu(args, world, rank, local):
     lse = torch.empty((P, B, Hg, S), dtype=torch.float32, device=dev)
     o_sh, dq_sh, dk_sh, dv_sh = (torch.empty_like(sh["q"]) for _ in range(4))
     ws = torch.empty(uaa.attn_bwd_workspace_bytes(P * B, S, Hg, D), dtype=torch.uint8, device=dev)
+    fused = args.path == "fused"
+    if fused:
+        # the exchanges fused into the attention kernels: the step reads and writes the shards only
+        lse_f = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        ws = torch.empty(uaa.ulysses_attn_bwd_workspace_bytes(lens, cap, B, H, D), dtype=torch.uint8, device=dev)
+        del yq, yk, yv, ydo, yo, ydq, ydk, ydv, lse
     stream = torch.cuda.current_stream(dev)
     ev = {}
     # per-call events around the backward's dK/dV and dQ kernels (created and recorded once up front)
@@ -266,7 +272,24 @@ def run_gpu(args, world, rank, local):
         e.record(stream)
         ev.setdefault(name, []).append(e)
 
+    def step_fused(timed=False, bufs=None):
+        src = bufs or sh
+        if timed:
+            mark("fwd0")
+        uaa.ulysses_attn_fwd(src["q"], src["k"], src["v"], lens, None, w.scale, out=o_sh, lse=lse_f)
+        if timed:
+            mark("fwd1")
+            mark("bwd0")
+            uaa.set_bwd_profile_events(next(prof_iter))
+        uaa.ulysses_attn_bwd(src["q"], src["k"], src["v"], o_sh, src["do"], lse_f, lens, None, w.scale, dq=dq_sh,
+                             dk=dk_sh, dv=dv_sh, workspace=ws)
+        if timed:
+            uaa.set_bwd_profile_events(None)
+            mark("bwd1")
+
     def step(timed=False):
+        if fused:
+            return step_fused(timed)
         if timed:
             mark("s2h_fwd0")
         for n, y in (("q", yq), ("k", yk), ("v", yv)):
@@ -302,7 +325,9 @@ def run_gpu(args, world, rank, local):
         if timed:
             mark("h2s_g1")
 
-    launches_per_step = 3 + 1 + 1 + 1 + 3 + 3
+    # exchange path: 3 seq->head, forward, head->seq (O), seq->head (dO), preprocess + dK/dV + dQ,
+    # 3 head->seq; fused path: padding fill + forward, 3 padding fills + preprocess + dK/dV + dQ
+    launches_per_step = (2 + 6) if fused else (3 + 1 + 1 + 1 + 3 + 3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -326,6 +351,9 @@ def run_gpu(args, world, rank, local):
     def pair_ms(a, b):
         return sum(x.elapsed_time(y) for x, y in zip(ev[a], ev[b]))
 
+    if fused:
+        for k in ("s2h_fwd0", "s2h_fwd1", "h2s_o0", "h2s_o1", "h2s_g0", "h2s_g1"):
+            ev[k] = []
     fwd_ms = pair_ms("fwd0", "fwd1") / args.steps
     bwd_ms = pair_ms("bwd0", "bwd1") / args.steps
     fwd_launch = pair_ms("fwd0", "fwd1") / len(ev["fwd0"])
@@ -334,6 +362,8 @@ def run_gpu(args, world, rank, local):
                    pair_ms("h2s_g0", "h2s_g1")) / args.steps
     tensor_bytes = B * S * H * D * 2
     relayout_bytes = 8 * 2 * tensor_bytes + 4 * (P * B * cap * H * D * 2 - tensor_bytes)  # + padding zero fill
+    if fused:
+        relayout_bytes = 0
     step_flops = flops(B, S, H, D)
     value = world * step_flops / (ms * 1e-3) / 1e12
 
@@ -386,6 +416,45 @@ def run_gpu(args, world, rank, local):
                 outs_host[n].copy_(t, non_blocking=True)
             e_g_out.record(d2h_s)
 
+    # fused path: the backward reads the input shards again, so two input buffer sets alternate and
+    # the next step's inputs arrive while this step computes
+    sh2 = {n: torch.empty_like(t) for n, t in sh.items()} if fused and not args.no_e2e else None
+    e_in_free = [torch.cuda.Event(), torch.cuda.Event()]
+    e_in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in e_in_free:
+        e.record(stream)
+    e2e_i = [0]
+
+    def e2e_step_fused():
+        i = e2e_i[0] % 2
+        e2e_i[0] += 1
+        bufs = sh if i == 0 else sh2
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(e_in_free[i])
+            for n in ("q", "k", "v", "do"):
+                bufs[n].copy_(host[n], non_blocking=True)
+            e_in_ready[i].record(h2d_s)
+        stream.wait_event(e_in_ready[i])
+        stream.wait_event(e_o_out)  # the previous step's read-back of O is done with o_sh
+        uaa.ulysses_attn_fwd(bufs["q"], bufs["k"], bufs["v"], lens, None, w.scale, out=o_sh, lse=lse_f)
+        e_o_ready.record(stream)
+        stream.wait_event(e_g_out)  # the previous step's read-back of the gradients is done
+        uaa.ulysses_attn_bwd(bufs["q"], bufs["k"], bufs["v"], o_sh, bufs["do"], lse_f, lens, None, w.scale,
+                             dq=dq_sh, dk=dk_sh, dv=dv_sh, workspace=ws)
+        e_in_free[i].record(stream)
+        e_g_ready.record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(e_o_ready)
+            outs_host["o"].copy_(o_sh, non_blocking=True)
+            e_o_out.record(d2h_s)
+            d2h_s.wait_event(e_g_ready)
+            for n, t in (("dq", dq_sh), ("dk", dk_sh), ("dv", dv_sh)):
+                outs_host[n].copy_(t, non_blocking=True)
+            e_g_out.record(d2h_s)
+
+    if fused:
+        e2e_step = e2e_step_fused  # noqa: F811
+
     e2e = None
     if not args.no_e2e:
         e2e_step()
@@ -433,6 +502,8 @@ def run_gpu(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name, "B": B, "N": S, "P": P, "H": H, "D": D, "shard_lens": list(lens),
                    "cap": cap, "mask": None, "l2": "inputs larger than L2 (4 x 279 MB shards), no flush",
+                   "path": "exchanges fused into the attention kernels" if fused else
+                   "seq->head / head->seq re-layout kernels around the attention kernels",
                    "parallelism": "replicas" if world > 1 else "single GPU, 4 emulated Ulysses ranks"},
         "parts_ms_per_step": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms, "relayout": relayout_ms},
         "attn_fwd_tflops": flops(B, S, H, D, bwd=False) / (fwd_ms * 1e-3) / 1e12,
@@ -441,8 +512,9 @@ def run_gpu(args, world, rank, local):
         "kernel_ms_per_launch": {"attn_fwd_kernel": fwd_launch, "attn_bwd_dkdv_kernel": dkdv_ms,
                                  "attn_bwd_dq_kernel": dq_ms},
         "dq_kernel_tflops": (6 * P * B * Hg * S * S * D) / (dq_ms * 1e-3) / 1e12,
-        "relayout_gbs": relayout_bytes / (relayout_ms * 1e-3) / 1e9,
-        "relayout_hbm_frac": (relayout_bytes / (relayout_ms * 1e-3) / 1e9) / peak_hbm if peak_hbm else None,
+        "relayout_gbs": relayout_bytes / (relayout_ms * 1e-3) / 1e9 if relayout_ms > 0 else None,
+        "relayout_hbm_frac": ((relayout_bytes / (relayout_ms * 1e-3) / 1e9) / peak_hbm
+                              if peak_hbm and relayout_ms > 0 else None),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -460,6 +532,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling-size variant)")
+    ap.add_argument("--path", default="exchange", choices=["fused", "exchange"],
+                    help="Ulysses step: attention kernels reading the shards directly, or separate re-layouts")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "uaa" else args.warmup
     if args.impl == "reference":

@@ -191,6 +191,52 @@ int uaa_seq_to_head(const void* x, void* y, int P, const int* shard_lens, int ca
 int uaa_head_to_seq(const void* y, void* x, int P, const int* shard_lens, int cap,
                     int B, int H, int D, int elem_bytes, uaa_stream_t stream);
 
+/* Ulysses attention with the exchanges fused into the attention kernels.
+ * "UAA-bwd", What does this PR do: seq->head all-to-all, attention on the head
+ * groups, head->seq all-to-all, with uneven shards; "fast-ulysses", Summary: the
+ * all-to-all time around the attention module is what the backend saves.  On
+ * one device the head groups together are all H heads, so the result is
+ *   out = head_to_seq(attention(seq_to_head(q), seq_to_head(k), seq_to_head(v)))
+ * computed without the re-layout round trips: the kernels read their 128-row
+ * tiles straight from the shards (one TMA tensor map per shard; a tile never
+ * straddles two shards, the last tile of a shard is partial) and write O back
+ * into the shards.
+ *   q, k, v, out : device, bf16 (P, B, cap, H, D) -- shard p's rows s < shard_lens[p]
+ *                  are the sequence positions off_p + s (off_p = sum of the
+ *                  earlier shard lengths); rows s >= shard_lens[p] are padding:
+ *                  never read, and written as zero in out
+ *   key_mask     : device uint8 (B, N) or NULL, N = sum(shard_lens), in sequence
+ *                  order (as built by uaa_assemble_key_mask)
+ *   lse          : device fp32 (B, H, N), sequence order
+ *   shard_lens   : host, P ints, 0 <= shard_lens[p] <= cap; 1 <= P <= 8
+ *                  (UAA_ERR_UNSUPPORTED otherwise; use the separate exchanges)
+ * The key tiling follows the shards, so the sums run in a different order than
+ * in uaa_attn_fwd on the re-laid-out tensors: results agree to rounding, not
+ * bit for bit.  Returns UAA_OK or a negative uaa_status. */
+int uaa_ulysses_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                         void* out, float* lse, int P, const int* shard_lens, int cap,
+                         int B, int H, int D, float scale, uaa_stream_t stream);
+
+/* Workspace for uaa_ulysses_attn_bwd: Delta and -LSE*log2(e) per query row,
+ * each (B, H, T*128) fp32 with T = sum over shards of ceil(shard_lens[p]/128),
+ * rounded up to 256 bytes.  Returns 0 for invalid arguments. */
+size_t uaa_ulysses_attn_bwd_workspace_bytes(int P, const int* shard_lens, int cap,
+                                            int B, int H, int D);
+
+/* Backward of uaa_ulysses_attn_fwd: dq, dk, dv (P, B, cap, H, D) from dout in the
+ * same sharded layout, with the exchanges fused the same way ("UAA-bwd", What
+ * does this PR do: dQ follows the query partition, dK/dV the key partition).
+ * Padding rows of dq, dk, dv are written as zero.  Deterministic (no atomics).
+ *   lse : the forward's (B, H, N); key_mask : the forward's mask or NULL
+ *   workspace : at least uaa_ulysses_attn_bwd_workspace_bytes() bytes, 256-byte
+ *               aligned; contents on entry are ignored
+ * Returns UAA_OK or a negative uaa_status. */
+int uaa_ulysses_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                         const void* dout, const float* lse, const uint8_t* key_mask,
+                         void* dq, void* dk, void* dv, int P, const int* shard_lens, int cap,
+                         int B, int H, int D, float scale, void* workspace, size_t workspace_bytes,
+                         uaa_stream_t stream);
+
 /* Key-padding mask assembly from gathered per-rank shards, trimming every
  * shard to its true length BEFORE concatenation ("UAA-bwd", What does this PR
  * do: the uneven mask-assembly fix; Validation: the four-rank masked case).

@@ -118,3 +118,24 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         uaa.attn_fwd(q, q, q)
+
+
+def test_fused_ulysses_rejects_bad_partitions_on_host(L):
+    fake = ctypes.c_void_p(1 << 20)
+    f = ctypes.c_float(0.1)
+    # more shards than the fused kernels take
+    lens9 = (ctypes.c_int * 9)(*([10] * 9))
+    assert L.uaa_ulysses_attn_fwd(fake, fake, fake, None, fake, fake, 9, lens9, 10, 1, 2, 128, f, None) == -2
+    assert "P=9" in _err()
+    # a shard longer than the capacity, a negative one, no lengths at all
+    bad = (ctypes.c_int * 2)(11, 5)
+    assert L.uaa_ulysses_attn_fwd(fake, fake, fake, None, fake, fake, 2, bad, 10, 1, 2, 128, f, None) == -1
+    neg = (ctypes.c_int * 2)(3, -1)
+    assert L.uaa_ulysses_attn_bwd(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, 2, neg, 10, 1, 2, 128,
+                                  f, fake, 1 << 20, None) == -1
+    assert L.uaa_ulysses_attn_fwd(fake, fake, fake, None, fake, fake, 2, None, 10, 1, 2, 128, f, None) == -1
+    # workspace: Delta and -LSE*log2e per row of every 128-row tile, tiles never straddling shards
+    ok = (ctypes.c_int * 3)(130, 1, 128)
+    tiles = 2 + 1 + 1
+    assert L.uaa_ulysses_attn_bwd_workspace_bytes(3, ok, 130, 2, 5, 64) == (2 * 5 * tiles * 128 * 8 + 255) // 256 * 256
+    assert L.uaa_ulysses_attn_bwd_workspace_bytes(9, lens9, 10, 1, 2, 128) == 0

@@ -55,6 +55,10 @@ _SIGS = {
                                 ctypes.c_size_t, _P]),
     "uaa_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
     "uaa_attn_bwd_noalloc_max_bytes": (ctypes.c_size_t, []),
+    "uaa_ulysses_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "uaa_ulysses_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _P, _I, _I, _I, _I]),
+    "uaa_ulysses_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float,
+                                  _P, ctypes.c_size_t, _P]),
     "uaa_seq_to_head": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "uaa_head_to_seq": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "uaa_assemble_key_mask": (_I, [_P, _P, _I, _P, _I, _I, _P]),
@@ -378,3 +382,102 @@ class UlyssesAttention(torch.autograd.Function):
 
 def ulysses_attention(q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):
     return UlyssesAttention.apply(q_sh, k_sh, v_sh, tuple(shard_lens), key_mask, scale)
+
+
+# --------------------------------------------------------------------------- Ulysses, exchanges fused
+def _shards(name, t, ref=None):
+    if t.dim() != 5:
+        raise ValueError(f"{name} must be (P, B, cap, H, D), got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (P, B, cap, H, D)")
+    if ref is not None and tuple(t.shape) != tuple(ref.shape):
+        raise ValueError(f"{name} shape {tuple(t.shape)} does not fit {tuple(ref.shape)}")
+
+
+def ulysses_attn_fwd(q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None, out=None, lse=None):
+    """``uaa_ulysses_attn_fwd``: Ulysses attention straight on the sequence shards.
+
+    ``q_sh``, ``k_sh``, ``v_sh``: ``(P, B, cap, H, D)`` bf16 shards; returns ``(out_sh, lse)`` with
+    ``out_sh`` in the same layout (padding rows zero) and ``lse`` fp32 ``(B, H, N)`` in sequence
+    order, N = sum(shard_lens).  ``key_mask`` is ``(B, N)`` in sequence order.
+    """
+    _shards("q_sh", q_sh)
+    _shards("k_sh", k_sh, q_sh)
+    _shards("v_sh", v_sh, q_sh)
+    _need_cuda(q_sh, k_sh, v_sh)
+    P, B, cap, H, D = q_sh.shape
+    arr, lens = _lens_array(shard_lens)
+    if len(lens) != P:
+        raise ValueError("len(shard_lens) must equal P")
+    N = sum(lens)
+    mask = normalize_key_mask(key_mask, B, N)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q_sh)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q_sh.device)
+    _check(lib().uaa_ulysses_attn_fwd(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(mask), _ptr(out), _ptr(lse), P, arr,
+                                      cap, B, H, D, float(scale), _P(_stream(q_sh.device))))
+    return out, lse
+
+
+def ulysses_attn_bwd_workspace_bytes(shard_lens, cap, B, H, D) -> int:
+    arr, lens = _lens_array(shard_lens)
+    return int(lib().uaa_ulysses_attn_bwd_workspace_bytes(len(lens), arr, cap, B, H, D))
+
+
+def ulysses_attn_bwd(q_sh, k_sh, v_sh, out_sh, dout_sh, lse, shard_lens, key_mask=None, scale=None, dq=None,
+                     dk=None, dv=None, workspace=None):
+    """``uaa_ulysses_attn_bwd``: the backward of :func:`ulysses_attn_fwd` on the shards."""
+    for n, t in (("k_sh", k_sh), ("v_sh", v_sh), ("out_sh", out_sh), ("dout_sh", dout_sh)):
+        _shards(n, t, q_sh)
+    _shards("q_sh", q_sh)
+    _need_cuda(q_sh, k_sh, v_sh, out_sh, dout_sh, lse)
+    P, B, cap, H, D = q_sh.shape
+    arr, lens = _lens_array(shard_lens)
+    if len(lens) != P:
+        raise ValueError("len(shard_lens) must equal P")
+    N = sum(lens)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 (B, H, N)")
+    mask = normalize_key_mask(key_mask, B, N)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q_sh) if dq is None else dq
+    dk = torch.empty_like(q_sh) if dk is None else dk
+    dv = torch.empty_like(q_sh) if dv is None else dv
+    nbytes = ulysses_attn_bwd_workspace_bytes(lens, cap, B, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q_sh.device)
+    wsb = workspace.numel() * workspace.element_size()
+    _check(lib().uaa_ulysses_attn_bwd(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(out_sh), _ptr(dout_sh), _ptr(lse),
+                                      _ptr(mask), _ptr(dq), _ptr(dk), _ptr(dv), P, arr, cap, B, H, D, float(scale),
+                                      _ptr(workspace), wsb, _P(_stream(q_sh.device))))
+    return dq, dk, dv
+
+
+class FusedUlyssesAttention(torch.autograd.Function):
+    """Ulysses attention with the exchanges fused into the attention kernels (same result as
+    :class:`UlyssesAttention` up to rounding; ``lse`` is ``(B, H, N)``, non-differentiable)."""
+
+    @staticmethod
+    def forward(ctx, q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):
+        out, lse = ulysses_attn_fwd(q_sh, k_sh, v_sh, shard_lens, key_mask, scale)
+        ctx.save_for_backward(q_sh, k_sh, v_sh, out, lse)
+        ctx.shard_lens, ctx.key_mask, ctx.scale = tuple(shard_lens), key_mask, scale
+        ctx.mark_non_differentiable(lse)
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, _dlse):
+        q_sh, k_sh, v_sh, out, lse = ctx.saved_tensors
+        dq, dk, dv = ulysses_attn_bwd(q_sh, k_sh, v_sh, out, dout.contiguous(), lse, ctx.shard_lens, ctx.key_mask,
+                                      ctx.scale)
+        return dq, dk, dv, None, None, None
+
+
+def ulysses_attention_fused(q_sh, k_sh, v_sh, shard_lens, key_mask=None, scale=None):
+    return FusedUlyssesAttention.apply(q_sh, k_sh, v_sh, tuple(shard_lens), key_mask, scale)

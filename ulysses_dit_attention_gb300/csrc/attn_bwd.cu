@@ -94,22 +94,25 @@ __device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity, const Dev
   if (!mbar_wait(bar, parity, ctx.timeout_ns)) atomicOr(ctx.status, kStatusTimeout);
 }
 
-// Warp-collective: the attended-key bits of key tile j (bit c of word t = key
-// 128j + 32t + c); keys past S count as masked.  Every lane gets all 4 words.
-__device__ __forceinline__ void key_tile_bits(const uint8_t* __restrict__ key_mask, int b, int S, int j,
+// Warp-collective: the attended-key bits of key tile j of sequence kd (bit c of
+// word t = key c' = 32t + c of the tile); keys past the tile's segment count as
+// masked.  Every lane gets all 4 words.  key_mask is (B, kd.total) in sequence order.
+__device__ __forceinline__ void key_tile_bits(const uint8_t* __restrict__ key_mask, const SeqDesc& kd, int b, int j,
                                               uint32_t (&w)[4]) {
   const int lane = threadIdx.x & 31;
+  const SeqTile kt = seq_tile(kd, j);
+  const size_t base = (size_t)b * kd.total + kd.off[kt.seg] + kt.row0;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const int key = j * kBT + 32 * t + lane;
-    const bool valid = key < S && (key_mask == nullptr || key_mask[(size_t)b * S + key] != 0);
+    const int c = 32 * t + lane;
+    const bool valid = c < kt.valid && (key_mask == nullptr || key_mask[base + c] != 0);
     w[t] = __ballot_sync(0xffffffffu, valid);
   }
 }
 
-__device__ __forceinline__ bool key_tile_any(const uint8_t* __restrict__ key_mask, int b, int S, int j) {
+__device__ __forceinline__ bool key_tile_any(const uint8_t* __restrict__ key_mask, const SeqDesc& kd, int b, int j) {
   uint32_t w[4];
-  key_tile_bits(key_mask, b, S, j, w);
+  key_tile_bits(key_mask, kd, b, j, w);
   return (w[0] | w[1] | w[2] | w[3]) != 0;
 }
 
@@ -140,25 +143,39 @@ __device__ __forceinline__ Item3 decode_item(int item, int ntiles, int H) {
 __device__ __forceinline__ uint32_t packed_a_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 // ---------------------------------------------------------------------------
-// 1. Delta = rowsum(dO * O).  Eight lanes per (b, s, h) row, 16-byte loads;
-// stored as (B, H, S).
+// 1. Delta = rowsum(dO * O) and -LSE*log2e per query row.  Eight lanes per
+// (b, position, h) row, 16-byte loads.  Stored per (b, h) in query-tile order:
+// row r of 128-row tile t of sequence qd at index t*128 + r of a (B, H, tiles*128)
+// array, the rows past each segment's end holding Delta = 0 and -inf.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
                                                              float* __restrict__ delta, float* __restrict__ nl2,
-                                                             int B, int S, int S_pad, int H) {
+                                                             const __grid_constant__ SeqDesc qd, int B, int H) {
   constexpr int kVecPerRow = D / 8;
   constexpr int kPerLane = kVecPerRow / 8;
+  const int S = qd.total;
+  const int S_pad = qd.tile0[qd.nseg] * 128;
   const size_t rows = (size_t)B * S * H;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t nthreads = (size_t)gridDim.x * blockDim.x;
   const int sub = threadIdx.x & 7;
   for (size_t r = tid >> 3; r < ((rows + 3) / 4) * 4; r += nthreads >> 3) {
+    // r = (b * S + n) * H + h, n a sequence position: row n - off[p] of segment p
+    const int h = (int)(r % H);
+    const size_t bn = r / H;
+    const int n = (int)(bn % S);
+    const int b = (int)(bn / S);
+    int p = 0;
+    if (r < rows)
+      while (p + 1 < qd.nseg && n >= qd.off[p + 1]) ++p;
+    const int sp = n - qd.off[p];
     float acc = 0.f;
     if (r < rows) {
-      const uint4* po = reinterpret_cast<const uint4*>(o + r * D);
-      const uint4* pd = reinterpret_cast<const uint4*>(dout + r * D);
+      const size_t e0 = seq_elem(qd, B, H, D, b, p, sp, h);
+      const uint4* po = reinterpret_cast<const uint4*>(o + e0);
+      const uint4* pd = reinterpret_cast<const uint4*>(dout + e0);
 #pragma unroll
       for (int t = 0; t < kPerLane; ++t) {
         const uint4 a = __ldg(po + sub + 8 * t);
@@ -178,22 +195,22 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     if (r < rows && sub == 0) {
-      const int h = (int)(r % H);
-      const size_t bs = r / H;
-      const int s = (int)(bs % S);
-      const int b = (int)(bs / S);
-      const float l = lse[((size_t)b * H + h) * S + s];
-      delta[((size_t)b * H + h) * S_pad + s] = acc;
-      nl2[((size_t)b * H + h) * S_pad + s] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+      const float l = lse[((size_t)b * H + h) * S + n];
+      const size_t w = ((size_t)b * H + h) * S_pad + (size_t)(qd.tile0[p] * 128 + sp);
+      delta[w] = acc;
+      nl2[w] = l == -INFINITY ? -INFINITY : -l * kLog2e;
     }
   }
-  // padding rows [S, S_pad) of every (b, h)
-  const int padn = S_pad - S;
-  for (size_t i = tid; i < (size_t)B * H * padn; i += nthreads) {
-    const size_t bh = i / padn;
-    const int s = S + (int)(i % padn);
-    delta[bh * S_pad + s] = 0.f;
-    nl2[bh * S_pad + s] = -INFINITY;
+  // the rows past each segment's end in its last tile, for every (b, h)
+  for (size_t i = tid; i < (size_t)B * H * S_pad; i += nthreads) {
+    const int row = (int)(i % S_pad);
+    const int t = row >> 7;
+    int p = 0;
+    while (p + 1 < qd.nseg && t >= qd.tile0[p + 1]) ++p;
+    if ((t - qd.tile0[p]) * 128 + (row & 127) >= qd.len[p]) {
+      delta[i] = 0.f;
+      nl2[i] = -INFINITY;
+    }
   }
 }
 
@@ -230,11 +247,12 @@ static_assert(sizeof(DkdvCtl) <= 256, "control block");
 
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+    attn_bwd_dkdv_kernel(const __grid_constant__ SegMaps tmQ, const __grid_constant__ SegMaps tmK,
+                         const __grid_constant__ SegMaps tmV, const __grid_constant__ SegMaps tmDO,
+                         const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
                          const float* __restrict__ nl2, const float* __restrict__ delta,
                          const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ dk,
-                         __nv_bfloat16* __restrict__ dv, int Sq, int Sk, int H, int num_items, float scale,
+                         __nv_bfloat16* __restrict__ dv, int B, int H, int num_items, float scale,
                          float scale_log2, DevCtx ctx) {
   using L = DkdvLayout<D>;
   constexpr int kChunks = D / 64;
@@ -254,8 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nkt = (Sk + kBT - 1) / kBT;  // key tiles: the work items
-  const int nqt = (Sq + kBT - 1) / kBT;  // query tiles: the inner loop
+  const int nkt = kd.tile0[kd.nseg];  // key tiles: the work items
+  const int nqt = qd.tile0[qd.nseg];  // query tiles: the inner loop
+  const int Sk = kd.total;
   const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
@@ -283,10 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmDO);
+    for (int p = 0; p < qd.nseg; ++p) {
+      tma_prefetch_desc(&tmQ.m[p]);
+      tma_prefetch_desc(&tmDO.m[p]);
+    }
+    for (int p = 0; p < kd.nseg; ++p) {
+      tma_prefetch_desc(&tmK.m[p]);
+      tma_prefetch_desc(&tmV.m[p]);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, 512);
@@ -306,22 +329,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nq = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) continue;
+      if (kMask && !key_tile_any(mask, kd, w.b, w.t)) continue;
       if (lane == 0) {
         if (it > 0) ok = wait_or_abort(&ctl->bar_kv_empty, (it - 1) & 1, ctx, ctl);
         if (ok) {
           mbar_arrive_expect_tx(&ctl->bar_kv_full, 2 * L::kTileBytes);
+          const SeqTile kt = seq_tile(kd, w.t);
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) {
-            tma_load_4d(smem + L::kK + c * kChunkBytes, &tmK, &ctl->bar_kv_full, c * 64, w.h, w.t * kBT, w.b);
-            tma_load_4d(smem + L::kV + c * kChunkBytes, &tmV, &ctl->bar_kv_full, c * 64, w.h, w.t * kBT, w.b);
+            tma_load_4d(smem + L::kK + c * kChunkBytes, &tmK.m[kt.seg], &ctl->bar_kv_full, c * 64, w.h, kt.row0, w.b);
+            tma_load_4d(smem + L::kV + c * kChunkBytes, &tmV.m[kt.seg], &ctl->bar_kv_full, c * 64, w.h, kt.row0, w.b);
           }
           kv_armed = it + 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const size_t row0 = ((size_t)w.b * H + w.h) * padded_rows(Sq);
+      const size_t row0 = ((size_t)w.b * H + w.h) * ((size_t)nqt * kBT);
+      SeqCursor qseg;  // query segment cursor
       for (int i = 0; ok && i < nqt; ++i, ++nq) {
+        const SeqTile qt = seq_tile_at(qd, i, qseg);
         const int qs = nq % L::kQStages;
         const uint32_t qu = nq / L::kQStages;
         const int ds = nq % L::kDStages;
@@ -334,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&ctl->bar_q_full[qs], L::kTileBytes + kBT * 4);
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(smem + L::kQ + qs * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full[qs], c * 64,
-                          w.h, i * kBT, w.b);
+              tma_load_4d(smem + L::kQ + qs * L::kTileBytes + c * kChunkBytes, &tmQ.m[qt.seg], &ctl->bar_q_full[qs],
+                          c * 64, w.h, qt.row0, w.b);
             bulk_load(sDelta + qs * kBT, delta + row0 + (size_t)i * kBT, kBT * 4, &ctl->bar_q_full[qs]);
             q_armed[qs] = qu + 1;
             if (du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
@@ -344,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes + kBT * 4);
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(smem + L::kDO + ds * L::kTileBytes + c * kChunkBytes, &tmDO, &ctl->bar_do_full[ds], c * 64,
-                          w.h, i * kBT, w.b);
+              tma_load_4d(smem + L::kDO + ds * L::kTileBytes + c * kChunkBytes, &tmDO.m[qt.seg],
+                          &ctl->bar_do_full[ds], c * 64, w.h, qt.row0, w.b);
             bulk_load(sLse + ds * kBT, nl2 + row0 + (size_t)i * kBT, kBT * 4, &ctl->bar_do_full[ds]);
             do_armed[ds] = du + 1;
           }
@@ -378,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = sbase + L::kV;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) continue;
+      if (kMask && !key_tile_any(mask, kd, w.b, w.t)) continue;
       if (lane == 0) {
         auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
         auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
@@ -452,19 +478,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute warps 0..7
-    const int qd = warp & 3;
+    const int quad = warp & 3;
     const int hf = warp >> 2;
-    const int jrow = qd * 32 + lane;  // key row = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+    const int jrow = quad * 32 + lane;  // key row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
     uint32_t nq = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      const int key = w.t * kBT + jrow;
-      if (kMask && !key_tile_any(mask, w.b, Sk, w.t)) {
+      const SeqTile kt = seq_tile(kd, w.t);
+      const bool kexists = jrow < kt.valid;  // key row kt.row0 + jrow of segment kt.seg
+      const size_t off = seq_elem(kd, B, H, D, w.b, kt.seg, kexists ? kt.row0 + jrow : 0, w.h) + hf * (D / 2);
+      if (kMask && !key_tile_any(mask, kd, w.b, w.t)) {
         // no attended key in this tile: dK = dV = 0
-        if (key < Sk) {
-          const size_t off = (((size_t)w.b * Sk + key) * H + w.h) * D + hf * (D / 2);
+        if (kexists) {
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             *reinterpret_cast<uint4*>(dk + off + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
@@ -473,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const bool kvalid = key < Sk && (!kMask || key_mask[(size_t)w.b * Sk + key] != 0);
+      const bool kvalid =
+          kexists && (!kMask || key_mask[(size_t)w.b * Sk + kd.off[kt.seg] + kt.row0 + jrow] != 0);
       for (int i = 0; i < nqt; ++i) {
         const uint32_t g = nq + i;
         const int qs = g % L::kQStages;
@@ -546,12 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_acc_done, it & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
-      const size_t off = (((size_t)w.b * Sk + key) * H + w.h) * D + hf * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
         tmem_ld32(tl + kColDV + hf * (D / 2) + 32 * c, gg);
-        if (key < Sk) {
+        if (kexists) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -563,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_ld32(tl + kColDK + hf * (D / 2) + 32 * c, gg);
-        if (key < Sk) {
+        if (kexists) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -628,11 +655,11 @@ static_assert(sizeof(DqCtl) <= 512, "control block");
 
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+    attn_bwd_dq_kernel(const __grid_constant__ SegMaps tmK, const __grid_constant__ SegMaps tmV,
+                       const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
                        const float* __restrict__ nl2g, const float* __restrict__ delta,
                        const uint8_t* __restrict__ key_mask, const __nv_bfloat16* __restrict__ qg,
-                       const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int Sq, int Sk, int H,
+                       const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int B, int H,
                        int num_items, float scale, float scale_log2, DevCtx ctx) {
   using L = DqLayout<D>;
   constexpr int kChunks = D / 64;
@@ -651,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nkt = (Sk + kBT - 1) / kBT;  // key tiles: the inner loop
-  const int nqt = (Sq + kBT - 1) / kBT;  // query tiles: the work items
+  const int nkt = kd.tile0[kd.nseg];  // key tiles: the inner loop
+  const int nqt = qd.tile0[qd.nseg];  // query tiles: the work items
   const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
@@ -674,10 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmDO);
+    for (int p = 0; p < kd.nseg; ++p) {
+      tma_prefetch_desc(&tmK.m[p]);
+      tma_prefetch_desc(&tmV.m[p]);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, 512);
@@ -697,10 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
+      SeqCursor kseg;  // key segment cursor (tiles are visited in order)
       for (int j = 0; ok && j < nkt; ++j) {
         uint32_t words[4] = {0u, 0u, 0u, 0u};
         if (kMask) {
-          key_tile_bits(mask, w.b, Sk, j, words);
+          key_tile_bits(mask, kd, w.b, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
 #pragma unroll
@@ -712,11 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
-            const CUtensorMap* map = kind == 0 ? &tmK : &tmV;
+            const SeqTile kt = seq_tile_at(kd, j, kseg);
+            const CUtensorMap* map = kind == 0 ? &tmK.m[kt.seg] : &tmV.m[kt.seg];
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
               tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + c * kChunkBytes, map,
-                          &ctl->bar_kv_full[slot], c * 64, w.h, j * kBT, w.b);
+                          &ctl->bar_kv_full[slot], c * 64, w.h, kt.row0, w.b);
             kv_armed[slot] = use + 1;
           }
         }
@@ -788,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the key tiles of this item, in order (all lanes evaluate the same mask)
       auto next_tile = [&](int from) {
         for (int jj = from; jj < nkt; ++jj)
-          if (!kMask || key_tile_any(mask, w.b, Sk, jj)) return jj;
+          if (!kMask || key_tile_any(mask, kd, w.b, jj)) return jj;
         return nkt;
       };
       int j = next_tile(0);
@@ -851,25 +880,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer waits for our hand-over
   } else {
     // ------------------------------------------------------------ compute warps 0..7
-    const int qd = warp & 3;
+    const int quad = warp & 3;
     const int hf = warp >> 2;
-    const int row = qd * 32 + lane;  // query row = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+    const int row = quad * 32 + lane;  // query row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
     uint32_t g = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
-      const int q = w.t * kBT + row;
+      const SeqTile qt = seq_tile(qd, w.t);
+      const bool qvalid = row < qt.valid;  // query row qt.row0 + row of segment qt.seg
+      const size_t qoff = seq_elem(qd, B, H, D, w.b, qt.seg, qvalid ? qt.row0 + row : 0, w.h);
       {
         // the previous item's MMAs have all completed (its dq_done was waited on)
-        const __nv_bfloat16* src = (hf == 0 ? qg : dog) + (((size_t)w.b * Sq + q) * H + w.h) * D;
+        const __nv_bfloat16* src = (hf == 0 ? qg : dog) + qoff;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           uint32_t wv[32];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (q < Sq) v = __ldg(reinterpret_cast<const uint4*>(src) + 8 * c + t);
+            if (qvalid) v = __ldg(reinterpret_cast<const uint4*>(src) + 8 * c + t);
             wv[4 * t + 0] = v.x;
             wv[4 * t + 1] = v.y;
             wv[4 * t + 2] = v.z;
@@ -880,15 +911,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&ctl->bar_qdo_ready);
       }
-      // rows past S read the padding (-inf, 0)
-      const size_t prow = ((size_t)w.b * H + w.h) * padded_rows(Sq) + q;
+      // rows past the segment read the padding (-inf, 0)
+      const size_t prow = ((size_t)w.b * H + w.h) * ((size_t)nqt * kBT) + (size_t)w.t * kBT + row;
       const float nl2 = nl2g[prow];
       const float dl = delta[prow];
       int ntiles = 0;
+      SeqCursor kseg;  // key segment cursor
       for (int j = 0; j < nkt; ++j) {
         uint32_t words[4];
         if (kMask) {
-          key_tile_bits(mask, w.b, Sk, j, words);
+          key_tile_bits(mask, kd, w.b, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
         // is there a next key tile?  Its K and V are read by the MMAs this tile's
@@ -897,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool has_next = j + 1 < nkt;
         if (kMask) {
           int jn = j + 1;
-          while (jn < nkt && !key_tile_any(mask, w.b, Sk, jn)) ++jn;
+          while (jn < nkt && !key_tile_any(mask, kd, w.b, jn)) ++jn;
           has_next = jn < nkt;
         }
         if (has_next) {
@@ -930,11 +962,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!((w0 >> c) & 1u)) p[c] = 0.f;
               if (!((w1 >> c) & 1u)) p[32 + c] = 0.f;
             }
-          } else if ((j + 1) * kBT > Sk) {
-            const int lim = Sk - j * kBT - 64 * hf;
+          } else {
+            // the last tile of a key segment is partial: its rows past the segment read as zeros
+            const int lim = seq_tile_at(kd, j, kseg).valid - 64 * hf;
+            if (lim < 64) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c >= lim) p[c] = 0.f;
+              for (int c = 0; c < 64; ++c)
+                if (c >= lim) p[c] = 0.f;
+            }
           }
         }
         ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dp_full, g & 1, ctx, ctl));
@@ -963,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_dq_done, it & 1, ctx, ctl));
       if (!ok) break;
       tc_fence_after();
-      __nv_bfloat16* drow = dq + (((size_t)w.b * Sq + q) * H + w.h) * D + hf * (D / 2);
+      __nv_bfloat16* drow = dq + qoff + hf * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
@@ -972,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 32; ++t) gg[t] = 0.f;
         }
-        if (q < Sq) {
+        if (qvalid) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -1034,50 +1069,64 @@ int record_prof(int i, cudaStream_t stream) {
 
 template <int D, bool kMask>
 int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
-               const uint8_t* mask, void* dq, void* dk, void* dv, int B, int Sq, int Sk, int H, float scale,
-               float* delta, cudaStream_t stream, const DevCtx& ctx) {
-  const size_t rows = (size_t)B * Sq * H;
-  float* nl2 = delta + (size_t)B * H * padded_rows(Sq);
+               const uint8_t* mask, void* dq, void* dk, void* dv, int B, const SeqDesc& qd, const SeqDesc& kd, int H,
+               float scale, float* delta, cudaStream_t stream, const DevCtx& ctx) {
+  const size_t rows = (size_t)B * qd.total * H;
+  const int nqt = qd.tile0[qd.nseg], nkt = kd.tile0[kd.nseg];
+  float* nl2 = delta + (size_t)B * H * nqt * kBT;
   bwd_preprocess_kernel<D><<<grid_cap(rows * 8, 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, nl2, B, Sq,
-      padded_rows(Sq), H);
+      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, nl2, qd, B, H);
   int st = check_launch("uaa_attn_bwd (preprocess)");
   if (st) return st;
-  CUtensorMap mq, mk, mv, mdo;
-  if ((st = encode_bshd_map(&mq, q, B, Sq, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mk, k, B, Sk, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mv, v, B, Sk, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mdo, dout, B, Sq, H, D, 128))) return st;
+  SegMaps mq, mk, mv, mdo;
+  if ((st = encode_seq_maps(&mq, q, qd, B, H, D, 128))) return st;
+  if ((st = encode_seq_maps(&mk, k, kd, B, H, D, 128))) return st;
+  if ((st = encode_seq_maps(&mv, v, kd, B, H, D, 128))) return st;
+  if ((st = encode_seq_maps(&mdo, dout, qd, B, H, D, 128))) return st;
   // dK/dV items are key tiles, dQ items are query tiles
-  const long long items_k = (long long)((Sk + kBT - 1) / kBT) * H * B;
-  const long long items_q = (long long)((Sq + kBT - 1) / kBT) * H * B;
+  const long long items_k = (long long)nkt * H * B;
+  const long long items_q = (long long)nqt * H * B;
   if (items_k > INT32_MAX || items_q > INT32_MAX)
     return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_bwd: too many work items");
   const int grid_k = (int)(items_k < sm_count() ? items_k : sm_count());
   const int grid_q = (int)(items_q < sm_count() ? items_q : sm_count());
   if ((st = record_prof(0, stream))) return st;
-  {
+  if (items_k > 0) {
     auto kern = attn_bwd_dkdv_kernel<D, kMask>;
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid_k, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<__nv_bfloat16*>(dk),
-                                             static_cast<__nv_bfloat16*>(dv), Sq, Sk, H, (int)items_k, scale,
-                                             scale * kLog2e, ctx);
+    kern<<<grid_k, kThreads, smem, stream>>>(mq, mk, mv, mdo, qd, kd, nl2, delta, mask,
+                                             static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), B, H,
+                                             (int)items_k, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
   }
   if ((st = record_prof(1, stream))) return st;
-  {
+  if (items_q > 0) {
     auto kern = attn_bwd_dq_kernel<D, kMask>;
     const int smem = DqLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid_q, kThreads, smem, stream>>>(mq, mk, mv, mdo, nl2, delta, mask, static_cast<const __nv_bfloat16*>(q),
+    kern<<<grid_q, kThreads, smem, stream>>>(mk, mv, qd, kd, nl2, delta, mask, static_cast<const __nv_bfloat16*>(q),
                                              static_cast<const __nv_bfloat16*>(dout), static_cast<__nv_bfloat16*>(dq),
-                                             Sq, Sk, H, (int)items_q, scale, scale * kLog2e, ctx);
+                                             B, H, (int)items_q, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dQ)"))) return st;
   }
   return record_prof(2, stream);
+}
+
+int bwd_dispatch(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                 const uint8_t* key_mask, void* dq, void* dk, void* dv, int B, const SeqDesc& qd, const SeqDesc& kd,
+                 int H, int D, float scale, float* delta, cudaStream_t s, const DevCtx& ctx) {
+  if (D == 64)
+    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta, s,
+                                           ctx)
+                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta,
+                                            s, ctx);
+  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta, s,
+                                          ctx)
+                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta, s,
+                                           ctx);
 }
 
 }  // namespace
@@ -1119,17 +1168,51 @@ extern "C" int uaa_attn_bwd_cross(const void* q, const void* k, const void* v, c
     return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
   DevCtx ctx;
   if ((st = get_dev_ctx(&ctx))) return st;
-  float* delta = static_cast<float*>(workspace);
+  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, seq_plain(Sq), seq_plain(Sk), H, D, scale,
+                      static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), ctx);
+}
+
+extern "C" size_t uaa_ulysses_attn_bwd_workspace_bytes(int P, const int* shard_lens, int cap, int B, int H, int D) {
+  SeqDesc sd;
+  if (B < 0 || H < 0 || (D != 64 && D != 128)) return 0;
+  if (seq_sharded(&sd, P, shard_lens, cap, "uaa_ulysses_attn_bwd_workspace_bytes")) return 0;
+  // Delta and -LSE*log2e, each (B, H, tiles * 128) fp32 in query-tile order
+  return (((size_t)B * H * sd.tile0[sd.nseg] * kBT * 8) + 255) & ~(size_t)255;
+}
+
+extern "C" int uaa_ulysses_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                    const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int P,
+                                    const int* shard_lens, int cap, int B, int H, int D, float scale, void* workspace,
+                                    size_t workspace_bytes, uaa_stream_t stream) {
+  const char* fn = "uaa_ulysses_attn_bwd";
+  SeqDesc sd;
+  int st = seq_sharded(&sd, P, shard_lens, cap, fn);
+  if (st) return st;
+  if ((st = validate_attn_sizes(fn, B, sd.total, sd.total, H, D, scale))) return st;
+  if ((uint64_t)B * H == 0) return UAA_OK;
+  if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
+      (st = check_dev_ptr(fn, "out", out)) || (st = check_dev_ptr(fn, "dout", dout)) ||
+      (st = check_dev_ptr(fn, "dq", dq)) || (st = check_dev_ptr(fn, "dk", dk)) || (st = check_dev_ptr(fn, "dv", dv)))
+    return st;
+  if ((uint64_t)P * B * cap * H * D * 4 >= (1ull << 40))
+    return set_error(UAA_ERR_UNSUPPORTED, "%s: tensor larger than the TMA stride range", fn);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 64)
-    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale, delta,
-                                           s, ctx)
-                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale,
-                                            delta, s, ctx);
-  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale, delta,
-                                          s, ctx)
-                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, Sq, Sk, H, scale, delta,
-                                           s, ctx);
+  // padding rows of the gradient shards are zero, as after the head->seq exchange
+  if ((st = zero_pad_rows(dq, sd, B, H, D, s)) || (st = zero_pad_rows(dk, sd, B, H, D, s)) ||
+      (st = zero_pad_rows(dv, sd, B, H, D, s)))
+    return st;
+  if (sd.total == 0) return UAA_OK;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: lse is NULL or not 4-byte aligned", fn);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: workspace is NULL or not 256-byte aligned", fn);
+  const size_t need = uaa_ulysses_attn_bwd_workspace_bytes(P, shard_lens, cap, B, H, D);
+  if (workspace_bytes < need)
+    return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
+  DevCtx ctx;
+  if ((st = get_dev_ctx(&ctx))) return st;
+  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, sd, sd, H, D, scale,
+                      static_cast<float*>(workspace), s, ctx);
 }
 
 extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,

@@ -42,7 +42,6 @@
 namespace uaa {
 namespace {
 
-constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kChunkBytes = 128 * 128;  // 128 rows x 128 bytes (one swizzle column block)
 constexpr int kThreads = 320;
@@ -133,10 +132,11 @@ __device__ __forceinline__ Item decode_item(int item, int nqp, int H) {
 
 template <int D, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const uint8_t* __restrict__ key_mask,
-                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int Sq, int Sk, int H, int num_items,
-                    float scale_log2, DevCtx ctx) {
+    attn_fwd_kernel(const __grid_constant__ SegMaps tmQ, const __grid_constant__ SegMaps tmK,
+                    const __grid_constant__ SegMaps tmV, const __grid_constant__ SeqDesc qd,
+                    const __grid_constant__ SeqDesc kd,
+                    const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                    int B, int H, int num_items, float scale_log2, DevCtx ctx) {
   using L = FwdLayout<D>;
   constexpr int kChunks = D / 64;
   constexpr int R = L::kRing;
@@ -155,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nqp = (Sq + 2 * kBM - 1) / (2 * kBM);
-  const int nkt = (Sk + kBN - 1) / kBN;
+  const int nqp = (qd.tile0[qd.nseg] + 1) / 2;  // query tile pairs (an item)
+  const int nkt = kd.tile0[kd.nseg];             // key tiles
+  const int Sk = kd.total;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->bar_q_full, 1);
@@ -175,9 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
+    for (int p = 0; p < qd.nseg; ++p) tma_prefetch_desc(&tmQ.m[p]);
+    for (int p = 0; p < kd.nseg; ++p) {
+      tma_prefetch_desc(&tmK.m[p]);
+      tma_prefetch_desc(&tmV.m[p]);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, 512);
@@ -205,16 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           mbar_arrive_expect_tx(&ctl->bar_q_full, 2 * L::kTileBytes);
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t) {
+            // a tile past the last one reads as zeros (rows past its segment) and is never written
+            const SeqTile qt = seq_tile(qd, 2 * w.qp + t);
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(smem + L::kQ + t * L::kTileBytes + c * kChunkBytes, &tmQ, &ctl->bar_q_full, c * 64, w.h,
-                          w.qp * 2 * kBM + t * kBM, w.b);
+              tma_load_4d(smem + L::kQ + t * L::kTileBytes + c * kChunkBytes, &tmQ.m[qt.seg], &ctl->bar_q_full,
+                          c * 64, w.h, qt.row0, w.b);
+          }
           q_armed = it + 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      SeqCursor kseg;  // key segment cursor (tiles are visited in order)
       for (int j = 0; ok && j < nkt; ++j) {
+        const SeqTile kt = seq_tile_at(kd, j, kseg);
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
           const int slot = n % R;
@@ -223,12 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (kMask && kind == 1) {
-            // bit c of word t = key j*128 + 32t + c is attended
+            // bit c of word t: key c' = 32t + c of the tile (sequence position
+            // off + row0 + c') exists and is attended
             uint32_t words[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-              const int key = j * kBN + 32 * t + lane;
-              const bool valid = key < Sk && key_mask[(size_t)w.b * Sk + key] != 0;
+              const int c = 32 * t + lane;
+              const bool valid = c < kt.valid && key_mask[(size_t)w.b * Sk + kd.off[kt.seg] + kt.row0 + c] != 0;
               words[t] = __ballot_sync(0xffffffffu, valid);
             }
             if (lane == 0) {
@@ -239,11 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
-            const CUtensorMap* map = kind == 0 ? &tmK : &tmV;
+            const CUtensorMap* map = kind == 0 ? &tmK.m[kt.seg] : &tmV.m[kt.seg];
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
               tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + c * kChunkBytes, map,
-                          &ctl->bar_kv_full[slot], c * 64, w.h, j * kBN, w.b);
+                          &ctl->bar_kv_full[slot], c * 64, w.h, kt.row0, w.b);
             kv_armed[slot] = use + 1;
           }
         }
@@ -354,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item w = decode_item(item, nqp, H);
       float mu = -INFINITY;  // log2-domain offset in use (scaled max, possibly stale by < 2^8)
       float l_run = 0.f;
+      SeqCursor kseg;  // key segment cursor
       for (int j = 0; j < nkt; ++j) {
         const uint32_t gj = g + j;
         if (ok) {
@@ -386,11 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
-        } else if ((j + 1) * kBN > Sk) {
-          const int lim = Sk - j * kBN;
+        } else {
+          // the last tile of a segment is partial: its rows past the segment read as zeros
+          const int lim = seq_tile_at(kd, j, kseg).valid;
+          if (lim < kBN) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= lim) s[c] = -INFINITY;
+            for (int c = 0; c < kBN; ++c)
+              if (c >= lim) s[c] = -INFINITY;
+          }
         }
         // row max over the tile: eight independent chains (the max sits on the
         // critical path between S_t and PV_t), then a short tree
@@ -449,14 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       tc_fence_after();
-      const int q = w.qp * 2 * kBM + t * kBM + row;
+      const SeqTile qt = seq_tile(qd, 2 * w.qp + t);
+      const bool qvalid = row < qt.valid;
+      const int qs = qt.row0 + row;  // row within the query segment
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = out + (((size_t)w.b * Sq + q) * H + w.h) * D;
+      __nv_bfloat16* orow = out + seq_elem(qd, B, H, D, w.b, qt.seg, qvalid ? qs : 0, w.h);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         tmem_ld32(tl + colO + 32 * c, o);
-        if (q < Sq) {
+        if (qvalid) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 v;
@@ -470,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&ctl->bar_o_free);
-      if (q < Sq) lse[((size_t)w.b * H + w.h) * Sq + q] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
+      if (qvalid)
+        lse[((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
       g += nkt;
     }
   }
@@ -509,23 +525,32 @@ int sm_count() {
 
 template <int D, bool kMask>
 int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, void* out, float* lse, int B,
-               int Sq, int Sk, int H, float scale, cudaStream_t stream, const DevCtx& ctx) {
-  CUtensorMap mq, mk, mv;
+               const SeqDesc& qd, const SeqDesc& kd, int H, float scale, cudaStream_t stream, const DevCtx& ctx) {
+  SegMaps mq, mk, mv;
   int st;
-  if ((st = encode_bshd_map(&mq, q, B, Sq, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mk, k, B, Sk, H, D, 128))) return st;
-  if ((st = encode_bshd_map(&mv, v, B, Sk, H, D, 128))) return st;
+  if ((st = encode_seq_maps(&mq, q, qd, B, H, D, 128))) return st;
+  if ((st = encode_seq_maps(&mk, k, kd, B, H, D, 128))) return st;
+  if ((st = encode_seq_maps(&mv, v, kd, B, H, D, 128))) return st;
   auto kern = attn_fwd_kernel<D, kMask>;
   const int smem = FwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_fwd: smem attribute: %s", cudaGetErrorString(e));
-  const long long nqp = (Sq + 2 * kBM - 1) / (2 * kBM);
+  const long long nqp = (qd.tile0[qd.nseg] + 1) / 2;
   const long long items = nqp * H * B;
   if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_fwd: too many work items");
   const int grid = (int)(items < sm_count() ? items : sm_count());
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mask, static_cast<__nv_bfloat16*>(out), lse, Sq, Sk, H, (int)items,
-                                         scale * kLog2e, ctx);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, qd, kd, mask, static_cast<__nv_bfloat16*>(out), lse, B, H,
+                                         (int)items, scale * kLog2e, ctx);
   return check_launch("uaa_attn_fwd");
+}
+
+int fwd_dispatch(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out, float* lse, int B,
+                 const SeqDesc& qd, const SeqDesc& kd, int H, int D, float scale, cudaStream_t s, const DevCtx& ctx) {
+  if (D == 64)
+    return key_mask ? launch_fwd<64, true>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx)
+                    : launch_fwd<64, false>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx);
+  return key_mask ? launch_fwd<128, true>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx)
+                  : launch_fwd<128, false>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx);
 }
 
 }  // namespace
@@ -568,15 +593,36 @@ extern "C" int uaa_attn_fwd_cross(const void* q, const void* k, const void* v, c
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return set_error(UAA_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
   DevCtx ctx;
   if ((st = get_dev_ctx(&ctx))) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 64)
-    return key_mask ? launch_fwd<64, true>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx)
-                    : launch_fwd<64, false>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx);
-  return key_mask ? launch_fwd<128, true>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx)
-                  : launch_fwd<128, false>(q, k, v, key_mask, out, lse, B, Sq, Sk, H, scale, s, ctx);
+  return fwd_dispatch(q, k, v, key_mask, out, lse, B, seq_plain(Sq), seq_plain(Sk), H, D, scale,
+                      static_cast<cudaStream_t>(stream), ctx);
 }
 
 extern "C" int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
                             float* lse, int B, int S, int H, int D, float scale, uaa_stream_t stream) {
   return uaa_attn_fwd_cross(q, k, v, key_mask, out, lse, B, S, S, H, D, scale, stream);
+}
+
+extern "C" int uaa_ulysses_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
+                                    float* lse, int P, const int* shard_lens, int cap, int B, int H, int D, float scale,
+                                    uaa_stream_t stream) {
+  const char* fn = "uaa_ulysses_attn_fwd";
+  SeqDesc sd;
+  int st = seq_sharded(&sd, P, shard_lens, cap, fn);
+  if (st) return st;
+  if ((st = validate_attn_sizes(fn, B, sd.total, sd.total, H, D, scale))) return st;
+  if ((uint64_t)B * H == 0) return UAA_OK;
+  if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
+      (st = check_dev_ptr(fn, "out", out)))
+    return st;
+  if (sd.total > 0 && !lse) return set_error(UAA_ERR_INVALID_ARG, "%s: lse is NULL", fn);
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return set_error(UAA_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
+  if ((uint64_t)P * B * cap * H * D * 4 >= (1ull << 40))
+    return set_error(UAA_ERR_UNSUPPORTED, "%s: tensor larger than the TMA stride range", fn);
+  DevCtx ctx;
+  if ((st = get_dev_ctx(&ctx))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // padding rows of the output shards are zero, as after the head->seq exchange
+  if ((st = zero_pad_rows(out, sd, B, H, D, s))) return st;
+  if (sd.total == 0) return UAA_OK;
+  return fwd_dispatch(q, k, v, key_mask, out, lse, B, sd, sd, H, D, scale, s, ctx);
 }

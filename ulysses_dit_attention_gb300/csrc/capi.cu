@@ -105,6 +105,63 @@ int encode_bshd_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, 
   return UAA_OK;
 }
 
+SeqDesc seq_plain(int S) {
+  SeqDesc d{};
+  d.nseg = 1;
+  d.cap = S;
+  d.total = S;
+  d.len[0] = S;
+  d.off[0] = 0;
+  d.tile0[0] = 0;
+  d.tile0[1] = (S + 127) / 128;
+  return d;
+}
+
+int seq_sharded(SeqDesc* d, int P, const int* lens, int cap, const char* fn) {
+  if (P < 1 || P > kMaxSeg)
+    return set_error(UAA_ERR_UNSUPPORTED, "%s: P=%d shards (the fused path takes 1..%d)", fn, P, kMaxSeg);
+  if (!lens) return set_error(UAA_ERR_INVALID_ARG, "%s: shard_lens is NULL", fn);
+  if (cap < 1) return set_error(UAA_ERR_INVALID_ARG, "%s: cap=%d", fn, cap);
+  *d = SeqDesc{};
+  d->nseg = P;
+  d->cap = cap;
+  long long total = 0, tiles = 0;
+  for (int p = 0; p < P; ++p) {
+    if (lens[p] < 0 || lens[p] > cap)
+      return set_error(UAA_ERR_INVALID_ARG, "%s: shard %d has %d rows (cap %d)", fn, p, lens[p], cap);
+    d->len[p] = lens[p];
+    d->off[p] = (int)total;
+    d->tile0[p] = (int)tiles;
+    total += lens[p];
+    tiles += (lens[p] + 127) / 128;
+  }
+  if (total > INT32_MAX / 2) return set_error(UAA_ERR_UNSUPPORTED, "%s: sequence too long", fn);
+  d->total = (int)total;
+  d->tile0[P] = (int)tiles;
+  return UAA_OK;
+}
+
+int encode_seq_maps(SegMaps* maps, const void* ptr, const SeqDesc& d, int B, int H, int D, int box_rows) {
+  if (!encoder()) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  *maps = SegMaps{};
+  for (int p = 0; p < d.nseg; ++p) {
+    // segment p: rows [0, len) of slabs p*B .. p*B+B-1; an empty segment gets a one-row map
+    // that no tile reads
+    const char* base = static_cast<const char*>(ptr) + (size_t)p * B * d.cap * H * D * 2;
+    const int rows = d.len[p] > 0 ? d.len[p] : 1;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)d.cap * H * D * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(&maps->m[p], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<char*>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled failed for segment %d (CUresult %d)", p, (int)r);
+  }
+  return UAA_OK;
+}
+
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // runs out and records a timeout.  No copy or tensor-core work is issued.
 __global__ void watchdog_selftest_kernel(DevCtx ctx) {

@@ -131,6 +131,21 @@ __global__ void __launch_bounds__(kThreads) assemble_key_mask_kernel(const uint8
   }
 }
 
+// x[z, s, :] = 0 for the padding rows len[p] <= s < cap of every slab z = p*B + b of a
+// (nseg*B, cap, H, D) bf16 buffer; one thread per 16-byte vector.
+__global__ void __launch_bounds__(kThreads) zero_pad_kernel(uint4* __restrict__ x, const SeqDesc d, int B,
+                                                            int rowvec, int maxpad, uint64_t total) {
+  const uint64_t per_slab = (uint64_t)maxpad * rowvec;
+  for (uint64_t idx = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t z = idx / per_slab;
+    const uint64_t i = idx - z * per_slab;
+    const int p = (int)(z / (uint64_t)B);
+    if (i < (uint64_t)(d.cap - d.len[p]) * rowvec)
+      x[(z * d.cap + d.len[p]) * rowvec + i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 int sm_count() {
   static int cached = 0;
   if (!cached) {
@@ -198,6 +213,17 @@ int relayout_common(const char* fn, const void* src, const void* dst, int P, con
 }
 
 }  // namespace
+
+int zero_pad_rows(void* x, const SeqDesc& d, int B, int H, int D, cudaStream_t stream) {
+  int maxpad = 0;
+  for (int p = 0; p < d.nseg; ++p) maxpad = d.cap - d.len[p] > maxpad ? d.cap - d.len[p] : maxpad;
+  if (maxpad == 0 || B == 0 || H == 0) return UAA_OK;
+  const int rowvec = H * D * 2 / 16;
+  const uint64_t total = (uint64_t)d.nseg * B * maxpad * rowvec;
+  zero_pad_kernel<<<grid_for(total, 1), kThreads, 0, stream>>>(static_cast<uint4*>(x), d, B, rowvec, maxpad, total);
+  return check_launch("zero_pad_rows");
+}
+
 }  // namespace uaa
 
 using namespace uaa;

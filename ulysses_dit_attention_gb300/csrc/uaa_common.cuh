@@ -36,6 +36,41 @@ int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int 
 // fp32 (B, S, H, D) tensor; box = 32 columns (128 bytes) x box_rows positions, 128-byte swizzle.
 int encode_bshd_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows);
 
+// ----------------------------------------------------------------------------
+// A sequence made of segments.  Segment p holds len[p] rows at rows [0, len[p])
+// of slab p*B + b (batch b) of a (nseg*B, cap, H, D) bf16 buffer, and its rows
+// follow those of segments 0..p-1 in the sequence: row s of segment p is
+// sequence position off[p] + s.  A plain (B, S, H, D) tensor is one segment
+// (len = cap = S).  The sequence-sharded inputs of a Ulysses step are P
+// segments: shard p holds the positions [off[p], off[p] + len[p]).
+// The attention kernels walk it in 128-row tiles that never straddle two
+// segments: tile t belongs to segment p with tile0[p] <= t < tile0[p+1] and
+// covers its rows (t - tile0[p])*128 .. +127, the last tile of a segment
+// being partial.
+// ----------------------------------------------------------------------------
+constexpr int kMaxSeg = 8;
+struct SeqDesc {
+  int nseg;
+  int cap;                 // rows per slab
+  int total;               // sequence length: sum of len
+  int len[kMaxSeg];
+  int off[kMaxSeg];
+  int tile0[kMaxSeg + 1];  // first 128-row tile of each segment; tile0[nseg] = number of tiles
+};
+// One tensor map per segment over its (B, len, H, D) rows, 64-column x
+// box_rows boxes, 128-byte swizzle: rows past len[p] read as zeros, so padding
+// rows of the slab never enter a tile.
+struct SegMaps {
+  CUtensorMap m[kMaxSeg];
+};
+// Host: the plain layout (B, S, H, D) as one segment.
+SeqDesc seq_plain(int S);
+// Host: P segments of the given lengths in slabs of cap rows; UAA_ERR_* on bad input.
+int seq_sharded(SeqDesc* d, int P, const int* lens, int cap, const char* fn);
+int encode_seq_maps(SegMaps* maps, const void* ptr, const SeqDesc& d, int B, int H, int D, int box_rows);
+// Host: write zeros to the padding rows [len[p], cap) of every slab of a (nseg*B, cap, H, D) bf16 buffer.
+int zero_pad_rows(void* x, const SeqDesc& d, int B, int H, int D, cudaStream_t stream);
+
 #if defined(__CUDACC__)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -379,5 +414,56 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+
+#if defined(__CUDACC__)
+// Segment of 128-row tile t (tile0[p] <= t < tile0[p+1]); t past the last tile maps to the
+// last segment, whose rows there read as zeros.
+__device__ __forceinline__ int seq_seg_of_tile(const SeqDesc& d, int t) {
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < d.nseg && t >= d.tile0[p + 1]) ++p;
+  return p;
+}
+// Position of tile t: its segment, its first row within the segment, and the number of
+// valid rows (0 past the end of the sequence).
+struct SeqTile {
+  int seg, row0, valid;
+};
+__device__ __forceinline__ SeqTile seq_tile(const SeqDesc& d, int t) {
+  SeqTile r;
+  r.seg = seq_seg_of_tile(d, t);
+  r.row0 = (t - d.tile0[r.seg]) * 128;
+  const int left = d.len[r.seg] - r.row0;
+  r.valid = left < 0 ? 0 : (left < 128 ? left : 128);
+  return r;
+}
+// seq_tile for loops that visit tiles in increasing order.  The cursor keeps the
+// current segment's first tile, end and length in registers and reloads them
+// from the descriptor only when a visit crosses into a later segment, so a visit
+// reads no memory (with one segment: never after the first).
+struct SeqCursor {
+  int seg = -1, first = 0, next = 0, len = 0;
+};
+__device__ __forceinline__ SeqTile seq_tile_at(const SeqDesc& d, int t, SeqCursor& c) {
+#pragma unroll 1
+  while (t >= c.next && c.seg + 1 < d.nseg) {
+    ++c.seg;
+    c.first = d.tile0[c.seg];
+    c.next = d.tile0[c.seg + 1];
+    c.len = d.len[c.seg];
+  }
+  SeqTile r;
+  r.seg = c.seg;
+  r.row0 = (t - c.first) * 128;
+  const int left = c.len - r.row0;
+  r.valid = left < 0 ? 0 : (left < 128 ? left : 128);
+  return r;
+}
+// Element offset of (batch b, segment row s of segment p, head h, column 0) in the slab buffer.
+__device__ __forceinline__ size_t seq_elem(const SeqDesc& d, int B, int H, int D, int b, int p, int s, int h) {
+  return ((((size_t)p * B + b) * d.cap + s) * H + h) * (size_t)D;
+}
+#endif
 
 }  // namespace uaa
