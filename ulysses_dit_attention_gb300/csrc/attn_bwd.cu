@@ -653,7 +653,9 @@ struct DqCtl {
 };
 static_assert(sizeof(DqCtl) <= 512, "control block");
 
-template <int D, bool kMask>
+// kSeg: the key or query sequence has more than one segment (the fused Ulysses
+// step); with one segment the per-tile addressing reduces to row 128j of map 0.
+template <int D, bool kMask, bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ SegMaps tmK, const __grid_constant__ SegMaps tmV,
                        const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
@@ -740,12 +742,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
-            const SeqTile kt = seq_tile_at(kd, j, kseg);
-            const CUtensorMap* map = kind == 0 ? &tmK.m[kt.seg] : &tmV.m[kt.seg];
+            int ms = 0, row0 = j * kBT;
+            if constexpr (kSeg) {
+              const SeqTile kt = seq_tile_at(kd, j, kseg);
+              ms = kt.seg;
+              row0 = kt.row0;
+            }
+            const CUtensorMap* map = kind == 0 ? &tmK.m[ms] : &tmV.m[ms];
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
               tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + c * kChunkBytes, map,
-                          &ctl->bar_kv_full[slot], c * 64, w.h, kt.row0, w.b);
+                          &ctl->bar_kv_full[slot], c * 64, w.h, row0, w.b);
             kv_armed[slot] = use + 1;
           }
         }
@@ -964,7 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             // the last tile of a key segment is partial: its rows past the segment read as zeros
-            const int lim = seq_tile_at(kd, j, kseg).valid - 64 * hf;
+            const int lim = (kSeg ? seq_tile_at(kd, j, kseg).valid
+                                  : ((j + 1) * kBT > kd.total ? kd.total - j * kBT : kBT)) - 64 * hf;
             if (lim < 64) {
 #pragma unroll
               for (int c = 0; c < 64; ++c)
@@ -1103,7 +1111,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
   }
   if ((st = record_prof(1, stream))) return st;
   if (items_q > 0) {
-    auto kern = attn_bwd_dq_kernel<D, kMask>;
+    auto kern = (qd.nseg > 1 || kd.nseg > 1) ? attn_bwd_dq_kernel<D, kMask, true> : attn_bwd_dq_kernel<D, kMask, false>;
     const int smem = DqLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));

@@ -130,7 +130,9 @@ __device__ __forceinline__ Item decode_item(int item, int nqp, int H) {
   return it;
 }
 
-template <int D, bool kMask>
+// kSeg: the key or query sequence has more than one segment (the fused Ulysses
+// step); with one segment the per-tile addressing reduces to row 128j of map 0.
+template <int D, bool kMask, bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ SegMaps tmQ, const __grid_constant__ SegMaps tmK,
                     const __grid_constant__ SegMaps tmV, const __grid_constant__ SeqDesc qd,
@@ -222,7 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       SeqCursor kseg;  // key segment cursor (tiles are visited in order)
       for (int j = 0; ok && j < nkt; ++j) {
-        const SeqTile kt = seq_tile_at(kd, j, kseg);
+        SeqTile kt;
+        if constexpr (kSeg) {
+          kt = seq_tile_at(kd, j, kseg);
+        } else {
+          kt.seg = 0;
+          kt.row0 = j * kBN;
+          kt.valid = Sk - kt.row0 < kBN ? Sk - kt.row0 : kBN;
+        }
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
           const int slot = n % R;
@@ -248,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
-            const CUtensorMap* map = kind == 0 ? &tmK.m[kt.seg] : &tmV.m[kt.seg];
+            const int ms = kSeg ? kt.seg : 0;
+            const CUtensorMap* map = kind == 0 ? &tmK.m[ms] : &tmV.m[ms];
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
               tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + c * kChunkBytes, map,
@@ -398,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
         } else {
           // the last tile of a segment is partial: its rows past the segment read as zeros
-          const int lim = seq_tile_at(kd, j, kseg).valid;
+          const int lim = kSeg ? seq_tile_at(kd, j, kseg).valid : ((j + 1) * kBN > Sk ? Sk - j * kBN : kBN);
           if (lim < kBN) {
 #pragma unroll
             for (int c = 0; c < kBN; ++c)
@@ -523,7 +533,7 @@ int sm_count() {
   return n;
 }
 
-template <int D, bool kMask>
+template <int D, bool kMask, bool kSeg>
 int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, void* out, float* lse, int B,
                const SeqDesc& qd, const SeqDesc& kd, int H, float scale, cudaStream_t stream, const DevCtx& ctx) {
   SegMaps mq, mk, mv;
@@ -531,7 +541,7 @@ int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask,
   if ((st = encode_seq_maps(&mq, q, qd, B, H, D, 128))) return st;
   if ((st = encode_seq_maps(&mk, k, kd, B, H, D, 128))) return st;
   if ((st = encode_seq_maps(&mv, v, kd, B, H, D, 128))) return st;
-  auto kern = attn_fwd_kernel<D, kMask>;
+  auto kern = attn_fwd_kernel<D, kMask, kSeg>;
   const int smem = FwdLayout<D>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_fwd: smem attribute: %s", cudaGetErrorString(e));
@@ -546,11 +556,15 @@ int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask,
 
 int fwd_dispatch(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out, float* lse, int B,
                  const SeqDesc& qd, const SeqDesc& kd, int H, int D, float scale, cudaStream_t s, const DevCtx& ctx) {
-  if (D == 64)
-    return key_mask ? launch_fwd<64, true>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx)
-                    : launch_fwd<64, false>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx);
-  return key_mask ? launch_fwd<128, true>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx)
-                  : launch_fwd<128, false>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx);
+  const bool seg = qd.nseg > 1 || kd.nseg > 1;
+#define UAA_FWD(DD, MM, SS) launch_fwd<DD, MM, SS>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx)
+  if (D == 64) {
+    if (seg) return key_mask ? UAA_FWD(64, true, true) : UAA_FWD(64, false, true);
+    return key_mask ? UAA_FWD(64, true, false) : UAA_FWD(64, false, false);
+  }
+  if (seg) return key_mask ? UAA_FWD(128, true, true) : UAA_FWD(128, false, true);
+  return key_mask ? UAA_FWD(128, true, false) : UAA_FWD(128, false, false);
+#undef UAA_FWD
 }
 
 }  // namespace
