@@ -26,7 +26,7 @@ Parity pins: every function here is pinned by ``tests/test_oracle.py``
 own float64 SDPA + autograd, central finite differences, invariants).  No
 function is "parity unpinned".
 
-Conventions (readings where the pages are silent, listed in the design doc):
+Conventions (readings of what the pages leave open):
 * tensors are BSHD ``(B, S, H, D)`` -- the forward op returns its output in
   BSHD ("double-transpose", description paragraph on the forward/backward op
   contract);
