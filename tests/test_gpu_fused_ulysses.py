@@ -5,9 +5,9 @@ GPU through the C ABI, against the fp64 oracle's own Ulysses composition
 The fused kernels read 128-row tiles straight from the sequence shards (a tile
 never straddles two shards, so the last tile of each shard is partial) and
 write O, dQ, dK, dV back into the shards.  The cases cover partial tiles in
-every shard, an empty shard, a shard of one row, a shard ending exactly on a
-tile boundary, P = 1 and the maximum P = 8, key masks, and the full-size
-uneven-shard Ulysses workload on sampled heads.
+every shard, empty shards (leading, inner, last), a shard of one row, shards
+ending exactly on a tile boundary, P = 1 and the maximum P = 8, key masks, and
+the full-size uneven-shard Ulysses workload on sampled heads.
 """
 import numpy as np
 import pytest
@@ -42,6 +42,9 @@ CASES = [
     (1, [300], 320, 1, 2, 64, None),                     # one shard with padding rows
     (8, [50, 50, 50, 50, 50, 50, 50, 33], 64, 1, 8, 128, None),  # the largest P
     (2, [129, 127], 130, 2, 2, 128, "prefix"),           # prefix key mask over the sequence
+    (2, [100, 0], 100, 1, 2, 128, None),                 # empty last shard: the pair's second query tile is past the end
+    (3, [0, 0, 70], 70, 2, 2, 64, "random"),             # empty leading shards
+    (2, [128, 256], 256, 1, 3, 128, None),               # every shard a whole number of tiles
 ]
 
 
