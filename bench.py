@@ -46,7 +46,7 @@ WORKLOAD = "ulysses_p4_n27280_h40_d128"
 # above): the ncu capture of the same launch at 2 heads per group (profiles/), scaled by the five
 # times as many work items; keyed by the SHA-256 prefix of the attn_bwd.cu it was taken on, so the
 # bench reports null once the kernel source has changed since.
-DKDV_TRAFFIC = {"08495795f45d0036": 5 * (226782208 + 83292160)}
+DKDV_TRAFFIC = {"3e6839845bb7ccbc": 5 * (226782208 + 83292160)}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

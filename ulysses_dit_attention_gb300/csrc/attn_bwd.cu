@@ -12,9 +12,9 @@
 // deterministic:
 //  1. bwd_preprocess_kernel: Delta_i = sum_d dO_id * O_id (fp32), which equals
 //     sum_j P_ij dP_ij, and -LSE_i*log2(e), both into the workspace as (B, H,
-//     S_pad) rows padded to a whole number of 128-row tiles (padding: Delta = 0,
-//     -LSE*log2e = -inf, so padded rows get P = 0), which the dK/dV producer
-//     copies into shared memory with one bulk copy per tile.
+//     tiles*128) rows in query-tile order (rows past the end of a segment:
+//     Delta = 0, -LSE*log2e = -inf, so they get P = 0), which the dK/dV
+//     producer copies into shared memory with one bulk copy per tile.
 //  2. attn_bwd_dkdv_kernel (K/V-tile-major): a persistent CTA takes a 128-key
 //     tile of one (batch, head) and loops over all 128-row query tiles:
 //        S^T  = K Q^T,  P^T = exp2(S^T*c - lse2)            (M = keys)
@@ -34,8 +34,15 @@
 //
 // Warp roles in both main kernels: warps 0-7 compute (TMEM lane quadrant =
 // warp % 4, column half = warp / 4), warp 8 TMA producer, warp 9 tcgen05
-// issuer and warp 10 a second issuer, the two taking turns burst by burst.  An MMA that overwrites TMEM columns an earlier MMA of the same
-// thread reads is issued after it: the MMAs of one thread execute in order.
+// issuer and warp 10 a second issuer, the two taking turns burst by burst.  An
+// MMA that overwrites TMEM columns an earlier MMA of the same thread reads is
+// issued after it: the MMAs of one thread execute in order.
+//
+// Query and key sequences are segmented (SeqDesc): a plain (B, S, H, D)
+// tensor is one segment; the sequence shards of a Ulysses step are P segments,
+// read and written in place (one TMA tensor map per segment; 128-row tiles
+// never straddle two segments, so the last tile of a segment is partial and
+// its missing rows read as zeros, with P = 0 for those keys and queries).
 #include <math.h>
 
 #include <mutex>

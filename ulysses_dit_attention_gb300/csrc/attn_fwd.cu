@@ -35,6 +35,11 @@
 // overwrites those columns.
 // TMEM columns: [0,128) S/P of tile 0, [128,256) S/P of tile 1, [256,256+D)
 // O of tile 0, [256+D,256+2D) O of tile 1.
+// Query and key sequences are segmented (SeqDesc): a plain (B, S, H, D)
+// tensor is one segment; the sequence shards of a Ulysses step are P segments,
+// read and written in place (one TMA tensor map per segment; 128-row tiles
+// never straddle two segments; keys past a segment's end are masked, query
+// rows past it are not written).
 #include <math.h>
 
 #include "uaa_common.cuh"
