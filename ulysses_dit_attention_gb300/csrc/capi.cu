@@ -77,34 +77,6 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows) {
-  if (!encoder()) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  // dims innermost first: D (contiguous), H, S, B; a box is 64 elements of D
-  // (one 128-byte swizzle row) x 1 head x box_rows positions x 1 batch.
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-  return UAA_OK;
-}
-
-int encode_bshd_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows) {
-  if (!encoder()) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4, (cuuint64_t)S * H * D * 4};
-  cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return set_error(UAA_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (CUresult %d)", (int)r);
-  return UAA_OK;
-}
-
 SeqDesc seq_plain(int S) {
   SeqDesc d{};
   d.nseg = 1;

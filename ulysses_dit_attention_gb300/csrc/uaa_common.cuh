@@ -32,9 +32,6 @@ struct DevCtx {
 int get_dev_ctx(DevCtx* ctx);           // returns UAA_OK or UAA_ERR_CUDA (message set)
 int set_error(int status, const char* fmt, ...);
 int check_launch(const char* what);     // cudaGetLastError -> UAA_ERR_CUDA
-int encode_bshd_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows);
-// fp32 (B, S, H, D) tensor; box = 32 columns (128 bytes) x box_rows positions, 128-byte swizzle.
-int encode_bshd_map_f32(CUtensorMap* map, const void* ptr, int B, int S, int H, int D, int box_rows);
 
 // ----------------------------------------------------------------------------
 // A sequence made of segments.  Segment p holds len[p] rows at rows [0, len[p])
