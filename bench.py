@@ -200,6 +200,170 @@ def cpu_cores():
     return os.cpu_count() or 1
 
 
+def valid_keys(w, inp):
+    """Sum over batches of the attended key count (S per batch without a mask)."""
+    if inp["mask"] is None:
+        return w.B * w.S
+    return int(inp["mask"].to(torch.int64).sum())
+
+
+def oracle_config(w, inp, seconds):
+    """Times the fp64 oracle's forward + backward on workload ``w``.
+
+    Heads are independent, so the oracle runs head by head (all batches, all
+    rows) until every head is done or ``seconds`` have passed; when it stopped
+    early the full time is extrapolated by the FLOPs done.  For a sequence too
+    long to finish one head within the budget, blocks of query rows of one head
+    are timed instead (rows are independent too).  Returns a dict for the JSON line.
+    """
+    import numpy as np
+
+    import oracle
+
+    f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    m = None if inp["mask"] is None else inp["mask"].numpy().astype(bool)
+    total = 14 * w.H * w.S * w.D * valid_keys(w, inp)
+    head_flops = total / w.H
+    # one head of the 27280-row sequence takes ~20 s on 16 cores: sample row blocks instead
+    if w.S > 8192:
+        f, t, desc = oracle_sample(inp, w, seconds=seconds)
+        return {"tflops": f / t / 1e12, "full_s": total / (f / t), "timed_s": t, "extrapolated": True,
+                "cores": cpu_cores(), "sample": desc}
+    done, heads = 0, 0
+    t0 = time.perf_counter()
+    for h in range(w.H):
+        q, k, v, do = (f64(inp[n][:, :, [h]]) for n in ("q", "k", "v", "do"))
+        oracle.attn_fwd(q, k, v, m, w.scale)
+        oracle.attn_bwd(q, k, v, do, m, w.scale)
+        done += head_flops
+        heads += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    t = time.perf_counter() - t0
+    full = heads == w.H
+    desc = (f"fp64 NumPy oracle, fwd+bwd of {heads} of {w.H} heads (all {w.B} batches, {w.S} query rows); "
+            f"FLOPs counted as 14*H*S*sum(valid keys)*D")
+    return {"tflops": done / t / 1e12, "full_s": t if full else total / (done / t), "timed_s": t,
+            "extrapolated": not full, "cores": cpu_cores(), "sample": desc}
+
+
+# The workloads timed beside the headline: the layout trap, the 1k DiT shape, the key-padding
+# mask case and the full 40-head DiT layer.  (The Ulysses emulation is the headline itself.)
+PER_CONFIG = ("layout_b2_s16_h16_d64", "dit_b2_s1024_h24_d64", "mask_b4_s4096_h24_d128",
+              "dit_b1_s27280_h40_d128")
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+def time_config(uaa, w, dev, warmup, iters):
+    """fwd, bwd and fwd+bwd of one workload through the C ABI, each captured once in a CUDA graph
+    and replayed: CUDA events around every replay, the L2 flushed (a 256 MB write) between replays
+    when the inputs fit in L2, median over ``iters`` replays; plus the backward's per-kernel split
+    from an eager call with the profiling events."""
+    inp = synth.make(w)
+    B, S, H, D = w.B, w.S, w.H, w.D
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    mask = None if inp["mask"] is None else inp["mask"].to(dev)
+    out, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, uaa.attn_bwd_workspace_bytes(B, S, H, D)), dtype=torch.uint8, device=dev)
+    in_bytes = 4 * q.numel() * q.element_size()
+    flush = in_bytes < 2 * (129 << 20)
+    scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def fwd():
+        uaa.attn_fwd(q, k, v, mask, w.scale, out=out, lse=lse)
+
+    def bwd():
+        uaa.attn_bwd(q, k, v, out, do, lse, mask, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def both():
+        fwd()
+        bwd()
+
+    for _ in range(2):  # eager warm-up: loads the library, caches the device context and attributes
+        both()
+    torch.cuda.synchronize()
+    uaa.check_device_status(dev)
+    stream = torch.cuda.Stream(dev)
+    graphs = {}
+    for name, fn in (("fwd", fwd), ("bwd", bwd), ("fwd_bwd", both)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[name] = g
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    ms = {}
+    for name, g in graphs.items():
+        for _ in range(warmup):
+            g.replay()
+        times = []
+        for _ in range(iters):
+            if flush:
+                scratch.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            g.replay()
+            e1.record(cur)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        ms[name] = statistics.median(a.elapsed_time(b) for a, b in times)
+    # per-kernel split of the backward (eager calls, profiling events around the dK/dV and dQ kernels)
+    trios = []
+    for _ in range(max(3, iters // 4)):
+        if flush:
+            scratch.fill_(1)
+        trio = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in trio:  # torch only times events it has recorded itself once
+            e.record(torch.cuda.current_stream(dev))
+        uaa.set_bwd_profile_events(trio)
+        bwd()
+        uaa.set_bwd_profile_events(None)
+        trios.append(trio)
+    torch.cuda.synchronize()
+    uaa.check_device_status(dev)
+    dkdv_ms = statistics.median(a.elapsed_time(b) for a, b, _ in trios)
+    dq_ms = statistics.median(b.elapsed_time(c) for _, b, c in trios)
+    del graphs
+    L = valid_keys(w, inp)
+    ffl, bfl = 4 * H * S * D * L, 10 * H * S * D * L
+    rec = {"B": B, "S": S, "H": H, "D": D, "masked": inp["mask"] is not None, "valid_keys": L,
+           "fwd_ms": ms["fwd"], "bwd_ms": ms["bwd"], "fwd_bwd_ms": ms["fwd_bwd"],
+           "fwd_tflops": ffl / (ms["fwd"] * 1e-3) / 1e12, "bwd_tflops": bfl / (ms["bwd"] * 1e-3) / 1e12,
+           "fwd_bwd_tflops": (ffl + bfl) / (ms["fwd_bwd"] * 1e-3) / 1e12,
+           "bwd_kernels_ms": {"attn_bwd_dkdv_kernel": dkdv_ms, "attn_bwd_dq_kernel": dq_ms},
+           "timing": (f"CUDA graph replays, median of {iters}, "
+                      + ("L2 flushed (256 MB write) before each replay" if flush else
+                         "inputs larger than L2, no flush"))}
+    del q, k, v, do, out, dq, dk, dv, lse, ws, scratch
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_configs(uaa, args, dev, local):
+    """One record per workload of PER_CONFIG: GPU times and fractions of the measured peaks, then the
+    oracle on the host cores (after the GPU part, so the clock record covers the GPU work only)."""
+    pk, src = peaks()
+    sus, _ = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops")
+    burst, _ = _peak_value(pk, "bf16_tflops")
+    recs = {}
+    with Clocks(local) as clk:
+        for name in PER_CONFIG:
+            w = synth.workload(name)
+            big = w.S * w.S * w.H * w.B > (1 << 32)
+            recs[name] = time_config(uaa, w, dev, warmup=3 if big else 10, iters=5 if big else 30)
+    for name in PER_CONFIG:
+        w = synth.workload(name)
+        r = recs[name]
+        for key in ("fwd", "bwd", "fwd_bwd"):
+            r[f"{key}_frac_sustained"] = r[f"{key}_tflops"] / sus if sus else None
+            r[f"{key}_frac_burst"] = r[f"{key}_tflops"] / burst if burst else None
+        if args.cpu_config_seconds > 0 and not args.no_cpu:
+            r["oracle"] = oracle_config(w, synth.make(w), args.cpu_config_seconds)
+    return {"workloads": recs, "peak_source": src, "peak_sustained_tflops": sus, "peak_burst_tflops": burst,
+            "clocks": clk.summary()}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -518,6 +682,9 @@ def run_gpu(args, world, rank, local):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if rank == 0 and world == 1 and not args.no_configs and not args.heads:
+        # the other workloads, each timed on its own after the headline (not part of its step)
+        line["per_config"] = run_configs(uaa, args, dev, local)
     if rank == 0:
         print(json.dumps(line))
 
@@ -531,6 +698,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload records of the layout, 1k DiT, masked and full-layer workloads")
+    ap.add_argument("--cpu-config-seconds", type=float, default=30.0,
+                    help="host-time budget of the oracle per workload record (0: skip)")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling-size variant)")
     ap.add_argument("--path", default="exchange", choices=["fused", "exchange"],
                     help="Ulysses step: attention kernels reading the shards directly, or separate re-layouts")

@@ -32,7 +32,12 @@
  *    last non-OK status of the calling thread is in uaa_last_error().
  *  - Device-side waits (mbarrier / TMA / tensor-core completion) are bounded.
  *    A wait that runs out records UAA_ERR_TIMEOUT in a device status word and
- *    the kernel returns; uaa_check_device_status() reports and clears it.
+ *    the kernel returns; uaa_check_device_status() reports and clears it.  The
+ *    give-up is scoped to the call whose wait ran out: its other CTAs and
+ *    kernels stop waiting too (their outputs are then incomplete), while later
+ *    calls run normally even before the status has been read.  The calls
+ *    themselves cannot see a timeout of their own kernels (they return before
+ *    the kernels run): only uaa_check_device_status() reports it.
  *
  * Pointer alignment: every device pointer must be 16-byte aligned (the TMA
  * loads and the 16-byte vector copies need it).
@@ -126,6 +131,29 @@ int uaa_attn_bwd_cross(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int Sq, int Sk, int H, int D,
                        float scale, void* workspace, size_t workspace_bytes, uaa_stream_t stream);
 
+/* Attention of the G head groups of one Ulysses step, launched together.
+ * "UAA-bwd", What does this PR do: after the seq->head exchange every rank runs
+ * the plain attention on its head group with the full key-padding mask; on one
+ * device the G groups are G batches of B sequences each, and all of them share
+ * the same B mask rows.
+ *   q, k, v, out : device, bf16 (G*B, S, H, D) -- batch g*B + b is sequence b of group g
+ *   key_mask     : device, uint8 (B, S) or NULL; batch g*B + b uses row b
+ *   lse          : device, fp32 (G*B, H, S)
+ * Equals G calls of uaa_attn_fwd, one per group, bit for bit.  G >= 1,
+ * G*B <= 65535.  Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_fwd_groups(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                        void* out, float* lse, int G, int B, int S, int H, int D, float scale,
+                        uaa_stream_t stream);
+
+/* Backward of uaa_attn_fwd_groups (same layouts; the mask rows are shared the
+ * same way).  workspace: at least uaa_attn_bwd_workspace_bytes(G*B, S, H, D)
+ * bytes, 256-byte aligned.  Equals G calls of uaa_attn_bwd bit for bit.
+ * Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_bwd_groups(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, const uint8_t* key_mask,
+                        void* dq, void* dk, void* dv, int G, int B, int S, int H, int D,
+                        float scale, void* workspace, size_t workspace_bytes, uaa_stream_t stream);
+
 /* Profiling aid (off by default; the pages have no counterpart): when the
  * three CUDA events (cudaEvent_t, created by the caller) are non-NULL, every
  * later uaa_attn_bwd call of the calling thread records `before_dkdv` just
@@ -151,7 +179,9 @@ void uaa_set_bwd_profile_events(void* before_dkdv, void* after_dkdv, void* after
  * allocates or frees device memory.
  *  - The first call on each device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
- *    stream capture begins.
+ *    stream capture begins.  The cached address is not refreshed after the
+ *    device is reset (cudaDeviceReset) or its primary context is destroyed and
+ *    re-created: do not use this entry point across such a reset.
  *  - All calls share the one array, which keeps the last call's contents.
  *    Calls whose kernels may overlap on the GPU (e.g. on two streams with no
  *    ordering between them) race on it and produce wrong gradients; order
@@ -260,6 +290,16 @@ int uaa_watchdog_selftest(unsigned int timeout_us, uaa_stream_t stream);
 /* Sets the bound (in milliseconds, default 4000) of every device-side wait in
  * the kernels launched afterwards by the calling process. 0 restores the default. */
 void uaa_set_wait_timeout_ms(unsigned int ms);
+
+/* Diagnostic for the abort paths (the pages have no counterpart; off by
+ * default): while n >= 0, the producer of every attention kernel launched
+ * afterwards skips its n-th ring load (counted from 0 in each CTA: the forward's
+ * and the dQ kernel's K/V tile loads, the dK/dV kernel's query-tile loads).
+ * Nothing ever fills that buffer, so the waits for it run out after the wait
+ * bound, the call's kernels give up through their abort paths and
+ * uaa_check_device_status() reports UAA_ERR_TIMEOUT.  No copy is ever issued
+ * with a bad address: the load is simply not issued.  n < 0 turns it off. */
+void uaa_debug_drop_load(int n);
 
 /* Thread-local, NUL-terminated message for the last non-OK status returned to
  * the calling thread ("" if none).  Owned by the library. */

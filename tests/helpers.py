@@ -32,9 +32,14 @@ def compare(name, got, ref, kind=None, magnitude_scaled=False):
 
     The max-abs bars are stated for the workloads (N(0,1) inputs, scale 1/sqrt(D)),
     whose outputs are O(1).  With ``magnitude_scaled`` (used for a non-default
-    softmax scale, where outputs grow to several units and one bf16 ULP alone is
-    ~0.03) the max-abs bar is multiplied by max(1, max|ref|): the same relative
-    accuracy.  The relative Frobenius bar is unchanged.
+    softmax scale or a single key, where outputs grow to several units) the
+    max-abs bar is multiplied by max(1, max|ref|): the same relative accuracy at
+    the tensor's magnitude.  A bar per element (the stated bar plus a bf16 ULP of
+    that element) does not fit: the error of an element comes from the bf16
+    rounding of the contraction's operands (P and dS), which can be much larger
+    than the element itself after cancellation -- at scale 0.37 a dQ element of
+    1.2 carries an error of 0.039 from dS entries of ~10.  The relative
+    Frobenius bar is unchanged.
     """
     kind = kind or name
     got = np.asarray(got, dtype=np.float64)

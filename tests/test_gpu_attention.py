@@ -87,6 +87,39 @@ def test_small_and_ragged_cases(B, S, H, D, kind):
         assert (f64(dq)[1] == 0).all() and (f64(dk)[1] == 0).all() and (f64(dv)[1] == 0).all()
 
 
+def tile_pattern_mask(B, S, patterns, seed):
+    """Key mask built per 128-key tile: pattern character 'x' = every key of the tile masked,
+    'p' = a random ~60 % of its keys attended, 'a' = all attended.  One pattern per batch."""
+    g = torch.Generator().manual_seed(seed)
+    m = torch.zeros((B, S), dtype=torch.uint8)
+    for b, pat in enumerate(patterns):
+        for t, c in enumerate(pat):
+            lo, hi = 128 * t, min(S, 128 * (t + 1))
+            if c == "a":
+                m[b, lo:hi] = 1
+            elif c == "p":
+                m[b, lo:hi] = (torch.rand(hi - lo, generator=g) < 0.6).to(torch.uint8)
+    return m
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fully_masked_key_tiles_between_attended_ones(D):
+    """Key tiles 1 and 3 hold no attended key while tiles 0, 2 and 4 are partly attended:
+    the forward skips the empty tiles and the dK/dV and dQ kernels walk around them, each
+    role on its own, so they must agree on which tiles exist.  A second batch has a
+    different pattern (its own tile count), a third none attended at all."""
+    B, S, H = 3, 640, 2
+    inp = synth.draw(B, S, H, D, seed=640 + D)
+    mask = tile_pattern_mask(B, S, ["pxpxp", "xxaxp", "xxxxx"], seed=D)
+    res = check_against_oracle(inp, mask, 1.0 / math.sqrt(D), label=f"interior-masked D{D}")
+    o, lse, dq, dk, dv = run_gpu(inp, 1.0 / math.sqrt(D), mask)
+    assert (f64(o)[2] == 0).all() and np.isneginf(f64(lse)[2]).all()
+    assert (f64(dq)[2] == 0).all() and (f64(dk)[2] == 0).all() and (f64(dv)[2] == 0).all()
+    for b, t in ((0, 1), (0, 3), (1, 0), (1, 1), (1, 3)):
+        assert (f64(dk)[b, 128 * t:128 * (t + 1)] == 0).all() and (f64(dv)[b, 128 * t:128 * (t + 1)] == 0).all()
+    assert res["o"][0] > 0  # the attended rows were compared against nonzero values
+
+
 def test_non_default_scale():
     # scale 0.37 (~3x 1/sqrt(64)) sharpens the softmax; gradients reach |dQ| ~ 6
     inp = synth.draw(1, 200, 2, 64, seed=7)
@@ -269,6 +302,81 @@ def test_ulysses_padded_heads_equal_the_unsharded_path():
     assert np.array_equal(bits(unshard(k_sh.grad)), bits(dk))
     assert np.array_equal(bits(unshard(v_sh.grad)), bits(dv))
     for p, L in enumerate(lens):
+        for t in (o_sh, q_sh.grad, k_sh.grad, v_sh.grad):
+            assert (bits(t[p, :, L:]) == 0).all()
+
+
+@pytest.mark.parametrize("D,masked", [(128, True), (64, False)])
+def test_grouped_launch_equals_one_call_per_group(D, masked):
+    """uaa_attn_fwd_groups / uaa_attn_bwd_groups: G head groups of B sequences in one launch,
+    the B mask rows shared by every group, equal G separate calls bit for bit."""
+    G, B, S, H = 3, 2, 300, 2
+    g = torch.Generator().manual_seed(33 + D)
+    q, k, v, do = (torch.randn((G, B, S, H, D), generator=g).to(torch.bfloat16).to(DEV) for _ in range(4))
+    mask = None
+    if masked:
+        mask = tile_pattern_mask(B, S, ["pxp", "app"], seed=3).to(DEV)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = uaa.attn_fwd_groups(q, k, v, mask, scale)
+    dq, dk, dv = uaa.attn_bwd_groups(q, k, v, o, do, lse, mask, scale)
+    uaa.check_device_status()
+    for gi in range(G):
+        o1, l1 = uaa.attn_fwd(q[gi], k[gi], v[gi], mask, scale)
+        g1 = uaa.attn_bwd(q[gi], k[gi], v[gi], o1, do[gi], l1, mask, scale)
+        assert np.array_equal(bits(o[gi]), bits(o1)) and np.array_equal(bits(lse[gi]), bits(l1))
+        for a, b in zip((dq, dk, dv), g1):
+            assert np.array_equal(bits(a[gi]), bits(b))
+    uaa.check_device_status()
+    # and one group against the oracle
+    m = None if mask is None else mask.cpu().numpy().astype(bool)
+    qq, kk, vv, dd = (f64(t[1]) for t in (q, k, v, do))
+    ro, rl = oracle.attn_fwd(qq, kk, vv, m, scale)
+    rdq, rdk, rdv = oracle.attn_bwd(qq, kk, vv, dd, m, scale)
+    compare("groups O", f64(o[1]), ro, "o")
+    compare("groups LSE", f64(lse[1]), rl, "lse")
+    compare("groups dQ", f64(dq[1]), rdq, "dq")
+    compare("groups dK", f64(dk[1]), rdk, "dk")
+    compare("groups dV", f64(dv[1]), rdv, "dv")
+
+
+def test_masked_ulysses_exchange_path_end_to_end():
+    """The masked Ulysses step through the separate exchanges ("[attention] Add Ulysses
+    Anything backward", Validation: the four-rank masked case): every emulated rank holds
+    its shard of the key-padding mask; the gathered shards are trimmed and concatenated
+    by uaa_assemble_key_mask, and the assembled mask drives the attention of every head
+    group (one launch for all groups) in the forward and the backward."""
+    lens, cap = (301, 300, 257, 130), 301
+    P, B, H, D = 4, 2, 8, 128
+    N = sum(lens)
+    inp = synth.draw(B, N, H, D, seed=4141)
+    g = torch.Generator().manual_seed(4142)
+    full_mask = (torch.rand((B, N), generator=g) < 0.7).to(torch.uint8)
+    full_mask[1, 301:601] = 0  # rank 1's whole shard masked for batch 1: whole key tiles skipped
+    scale = 1.0 / math.sqrt(D)
+    mask_sh = oracle.split_key_mask(full_mask.numpy().astype(bool), lens, cap)  # (P, B, cap) per-rank shards
+    gathered = torch.from_numpy(mask_sh.astype(np.uint8)).to(DEV)
+    key_mask = uaa.assemble_key_mask(gathered, lens)
+    assert torch.equal(key_mask.cpu(), full_mask)
+    sh = {n: synth.pad_shards(inp[n], lens, cap).to(DEV) for n in ("q", "k", "v", "do")}
+    q_sh = sh["q"].requires_grad_(True)
+    k_sh = sh["k"].requires_grad_(True)
+    v_sh = sh["v"].requires_grad_(True)
+    o_sh, lse_g = uaa.ulysses_attention(q_sh, k_sh, v_sh, lens, key_mask, scale)
+    o_sh.backward(sh["do"])
+    uaa.check_device_status()
+    q, k, v, do = (f64(synth.pad_shards(inp[n], lens, cap)) for n in ("q", "k", "v", "do"))
+    ro, rl = oracle.ulysses_attn_fwd(q, k, v, lens, cap, mask_sh, scale)
+    rdq, rdk, rdv = oracle.ulysses_attn_bwd(q, k, v, do, lens, cap, mask_sh, scale)
+    compare("masked ulysses O", f64(o_sh.detach()), ro, "o")
+    compare("masked ulysses LSE", f64(lse_g), rl, "lse")
+    compare("masked ulysses dQ", f64(q_sh.grad), rdq, "dq")
+    compare("masked ulysses dK", f64(k_sh.grad), rdk, "dk")
+    compare("masked ulysses dV", f64(v_sh.grad), rdv, "dv")
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    for p, L in enumerate(lens):
+        mp = full_mask.numpy().astype(bool)[:, offs[p]:offs[p] + L]
+        for t in (k_sh.grad, v_sh.grad):
+            assert (f64(t[p, :, :L])[~mp] == 0).all()
         for t in (o_sh, q_sh.grad, k_sh.grad, v_sh.grad):
             assert (bits(t[p, :, L:]) == 0).all()
 

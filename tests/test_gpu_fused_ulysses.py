@@ -45,6 +45,8 @@ CASES = [
     (2, [100, 0], 100, 1, 2, 128, None),                 # empty last shard: the pair's second query tile is past the end
     (3, [0, 0, 70], 70, 2, 2, 64, "random"),             # empty leading shards
     (2, [128, 256], 256, 1, 3, 128, None),               # every shard a whole number of tiles
+    (3, [200, 300, 140], 300, 2, 2, 128, "holes"),       # whole key tiles masked inside shards 1 and 2
+    (3, [200, 300, 140], 300, 1, 2, 64, "holes"),
 ]
 
 
@@ -60,6 +62,13 @@ def test_fused_ulysses_matches_the_oracle(P, lens, cap, B, H, D, kind):
         mask = (torch.rand((B, N), generator=g) < 0.7).to(torch.uint8)
     elif kind == "prefix":
         mask = (torch.arange(N)[None, :] < torch.tensor([N // 2 + 3, N])[:B, None]).to(torch.uint8)
+    elif kind == "holes":
+        # the first tile of shard 1 (positions 200..327) and of shard 2 (500..627) hold no
+        # attended key, between partly attended tiles
+        g = torch.Generator().manual_seed(N + 1)
+        mask = (torch.rand((B, N), generator=g) < 0.7).to(torch.uint8)
+        mask[:, 200:328] = 0
+        mask[:, 500:628] = 0
     dsh = {n: t.to(DEV) for n, t in sh.items()}
     dmask = None if mask is None else mask.to(DEV)
     o_sh, lse = uaa.ulysses_attn_fwd(dsh["q"], dsh["k"], dsh["v"], lens, dmask, scale)

@@ -25,8 +25,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "seq_to_head", "head_to_seq",
-    "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms",
-    "set_bwd_profile_events", "Attention",
+    "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms", "debug_drop_load",
+    "set_bwd_profile_events", "Attention", "attn_fwd_groups", "attn_bwd_groups",
     "attention", "UlyssesAttention", "ulysses_attention", "STATUS",
 ]
 
@@ -53,6 +53,9 @@ _SIGS = {
                           ctypes.c_size_t, _P]),
     "uaa_attn_bwd_cross": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P,
                                 ctypes.c_size_t, _P]),
+    "uaa_attn_fwd_groups": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "uaa_attn_bwd_groups": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P,
+                                 ctypes.c_size_t, _P]),
     "uaa_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
     "uaa_attn_bwd_noalloc_max_bytes": (ctypes.c_size_t, []),
     "uaa_ulysses_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
@@ -65,6 +68,7 @@ _SIGS = {
     "uaa_check_device_status": (_I, [_P]),
     "uaa_watchdog_selftest": (_I, [ctypes.c_uint, _P]),
     "uaa_set_wait_timeout_ms": (None, [ctypes.c_uint]),
+    "uaa_debug_drop_load": (None, [_I]),
     "uaa_set_bwd_profile_events": (None, [_P, _P, _P]),
     "uaa_last_error": (ctypes.c_char_p, []),
     "uaa_version": (ctypes.c_char_p, []),
@@ -217,6 +221,65 @@ def attn_bwd(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=Non
     return dq, dk, dv
 
 
+def _groups(name, t, ref=None):
+    if t.dim() != 5:
+        raise ValueError(f"{name} must be (G, B, S, H, D), got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (G, B, S, H, D)")
+    if ref is not None and tuple(t.shape) != tuple(ref.shape):
+        raise ValueError(f"{name} shape {tuple(t.shape)} does not fit {tuple(ref.shape)}")
+
+
+def attn_fwd_groups(q, k, v, key_mask=None, scale=None, out=None, lse=None):
+    """``uaa_attn_fwd_groups``: attention of G head groups ``(G, B, S, H, D)`` in one launch.
+
+    The ``(B, S)`` key mask is shared by the G groups.  Returns ``(out, lse)`` with ``lse``
+    fp32 ``(G, B, H, S)``.
+    """
+    _groups("q", q)
+    _groups("k", k, q)
+    _groups("v", v, q)
+    _need_cuda(q, k, v)
+    G, B, S, H, D = q.shape
+    mask = normalize_key_mask(key_mask, B, S)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((G, B, H, S), dtype=torch.float32, device=q.device)
+    _check(lib().uaa_attn_fwd_groups(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), G, B, S, H, D,
+                                     float(scale), _P(_stream(q.device))))
+    return out, lse
+
+
+def attn_bwd_groups(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """``uaa_attn_bwd_groups``: the backward of :func:`attn_fwd_groups`; returns ``(dq, dk, dv)``."""
+    for n, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _groups(n, t, q)
+    _groups("q", q)
+    _need_cuda(q, k, v, out, dout, lse)
+    G, B, S, H, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (G, B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 (G, B, H, S)")
+    mask = normalize_key_mask(key_mask, B, S)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    nbytes = attn_bwd_workspace_bytes(G * B, S, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    wsb = workspace.numel() * workspace.element_size()
+    _check(lib().uaa_attn_bwd_groups(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), G, B, S, H, D, float(scale), _ptr(workspace), wsb,
+                                     _P(_stream(q.device))))
+    return dq, dk, dv
+
+
 class Attention(torch.autograd.Function):
     """Autograd pairing of ``attn_fwd`` / ``attn_bwd``; ``lse`` is non-differentiable."""
 
@@ -318,6 +381,12 @@ def set_wait_timeout_ms(ms: int):
     lib().uaa_set_wait_timeout_ms(int(ms))
 
 
+
+def debug_drop_load(n: int):
+    """Diagnostic: the attention kernels' producers skip their n-th ring load (-1: off)."""
+    lib().uaa_debug_drop_load(int(n))
+
+
 def set_bwd_profile_events(events=None):
     """Record three ``torch.cuda.Event``s around the backward's dK/dV and dQ kernels (None stops)."""
     if events is None:
@@ -328,11 +397,6 @@ def set_bwd_profile_events(events=None):
 
 
 # --------------------------------------------------------------------------- Ulysses composition
-def _flat(t):
-    """(P, B, N, Hg, D) head groups as one BSHD tensor of batch P*B (a view, no copy)."""
-    return t.flatten(0, 1)
-
-
 class UlyssesAttention(torch.autograd.Function):
     """Ulysses attention over P emulated ranks on one device.
 
@@ -348,14 +412,9 @@ class UlyssesAttention(torch.autograd.Function):
         cap, H = q_sh.shape[2], q_sh.shape[3]
         yq, yk, yv = (seq_to_head(t, shard_lens) for t in (q_sh, k_sh, v_sh))
         P = yq.shape[0]
-        o = torch.empty_like(yq)
-        lse = torch.empty((P, yq.shape[1], yq.shape[3], yq.shape[2]), dtype=torch.float32, device=yq.device)
-        if key_mask is None:
-            # the P groups form one BSHD tensor of batch P*B: one launch for all emulated ranks
-            attn_fwd(_flat(yq), _flat(yk), _flat(yv), None, scale, out=_flat(o), lse=lse.flatten(0, 1))
-        else:
-            for g in range(P):
-                attn_fwd(yq[g], yk[g], yv[g], key_mask, scale, out=o[g], lse=lse[g])
+        # the P groups form one batch of P*B sequences sharing the B mask rows: one launch for all
+        # emulated ranks
+        o, lse = attn_fwd_groups(yq, yk, yv, key_mask, scale)
         o_sh = head_to_seq(o, shard_lens, cap, H)
         ctx.save_for_backward(yq, yk, yv, o, lse)
         ctx.shard_lens, ctx.key_mask, ctx.scale, ctx.cap, ctx.H = tuple(shard_lens), key_mask, scale, cap, H
@@ -366,16 +425,7 @@ class UlyssesAttention(torch.autograd.Function):
     def backward(ctx, do_sh, _dlse):
         yq, yk, yv, o, lse = ctx.saved_tensors
         ydo = seq_to_head(do_sh.contiguous(), ctx.shard_lens)
-        P = yq.shape[0]
-        dq, dk, dv = torch.empty_like(yq), torch.empty_like(yq), torch.empty_like(yq)
-        if ctx.key_mask is None:
-            attn_bwd(_flat(yq), _flat(yk), _flat(yv), _flat(o), _flat(ydo), lse.flatten(0, 1), None, ctx.scale,
-                     dq=_flat(dq), dk=_flat(dk), dv=_flat(dv))
-        else:
-            ws = torch.empty(attn_bwd_workspace_bytes(*yq[0].shape), dtype=torch.uint8, device=yq.device)
-            for g in range(P):
-                attn_bwd(yq[g], yk[g], yv[g], o[g], ydo[g], lse[g], ctx.key_mask, ctx.scale, dq=dq[g], dk=dk[g],
-                         dv=dv[g], workspace=ws)
+        dq, dk, dv = attn_bwd_groups(yq, yk, yv, o, ydo, lse, ctx.key_mask, ctx.scale)
         return (head_to_seq(dq, ctx.shard_lens, ctx.cap, ctx.H), head_to_seq(dk, ctx.shard_lens, ctx.cap, ctx.H),
                 head_to_seq(dv, ctx.shard_lens, ctx.cap, ctx.H), None, None, None)
 

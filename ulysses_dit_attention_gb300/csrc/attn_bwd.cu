@@ -75,31 +75,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <typename Ctl>
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const DevCtx& ctx, Ctl* ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-    if (*reinterpret_cast<volatile unsigned int*>(ctx.status) & kStatusTimeout) {
-      // another CTA already gave up: stop waiting (the launch has failed)
-      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-      return false;
-    }
-    if (globaltimer_ns() - t0 > ctx.timeout_ns) {
-      atomicOr(ctx.status, kStatusTimeout);
-      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity, const DevCtx& ctx) {
-  if (!mbar_wait(bar, parity, ctx.timeout_ns)) atomicOr(ctx.status, kStatusTimeout);
-}
 
 // Warp-collective: the attended-key bits of key tile j of sequence kd (bit c of
 // word t = key c' = 32t + c of the tile); keys past the tile's segment count as
@@ -258,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ SegMaps tmV, const __grid_constant__ SegMaps tmDO,
                          const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
                          const float* __restrict__ nl2, const float* __restrict__ delta,
-                         const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ dk,
+                         const uint8_t* __restrict__ key_mask, int mrows, __nv_bfloat16* __restrict__ dk,
                          __nv_bfloat16* __restrict__ dv, int B, int H, int num_items, float scale,
                          float scale_log2, DevCtx ctx) {
   using L = DkdvLayout<D>;
@@ -336,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nq = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      if (kMask && !key_tile_any(mask, kd, w.b, w.t)) continue;
+      if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) continue;
       if (lane == 0) {
         if (it > 0) ok = wait_or_abort(&ctl->bar_kv_empty, (it - 1) & 1, ctx, ctl);
         if (ok) {
@@ -363,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Q_i with its Delta row, then dO_i with its -LSE*log2e row (rows past S
           // were written as Delta = 0 and -inf by the preprocess kernel)
           if (qu > 0) ok = wait_or_abort(&ctl->bar_q_empty[qs], (qu - 1) & 1, ctx, ctl);
-          if (ok) {
+          if (ok && (int)nq != ctx.drop_load) {
             mbar_arrive_expect_tx(&ctl->bar_q_full[qs], L::kTileBytes + kBT * 4);
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
@@ -371,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           c * 64, w.h, qt.row0, w.b);
             bulk_load(sDelta + qs * kBT, delta + row0 + (size_t)i * kBT, kBT * 4, &ctl->bar_q_full[qs]);
             q_armed[qs] = qu + 1;
-            if (du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
           }
+          if (ok && du > 0) ok = wait_or_abort(&ctl->bar_do_empty[ds], (du - 1) & 1, ctx, ctl);
           if (ok) {
             mbar_arrive_expect_tx(&ctl->bar_do_full[ds], L::kTileBytes + kBT * 4);
 #pragma unroll
@@ -411,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = sbase + L::kV;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
-      if (kMask && !key_tile_any(mask, kd, w.b, w.t)) continue;
+      if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) continue;
       if (lane == 0) {
         auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
         auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
@@ -496,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const SeqTile kt = seq_tile(kd, w.t);
       const bool kexists = jrow < kt.valid;  // key row kt.row0 + jrow of segment kt.seg
       const size_t off = seq_elem(kd, B, H, D, w.b, kt.seg, kexists ? kt.row0 + jrow : 0, w.h) + hf * (D / 2);
-      if (kMask && !key_tile_any(mask, kd, w.b, w.t)) {
+      if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) {
         // no attended key in this tile: dK = dV = 0
         if (kexists) {
 #pragma unroll
@@ -508,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const bool kvalid =
-          kexists && (!kMask || key_mask[(size_t)w.b * Sk + kd.off[kt.seg] + kt.row0 + jrow] != 0);
+          kexists && (!kMask || key_mask[(size_t)(w.b % mrows) * Sk + kd.off[kt.seg] + kt.row0 + jrow] != 0);
       for (int i = 0; i < nqt; ++i) {
         const uint32_t g = nq + i;
         const int qs = g % L::kQStages;
@@ -667,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ SegMaps tmK, const __grid_constant__ SegMaps tmV,
                        const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
                        const float* __restrict__ nl2g, const float* __restrict__ delta,
-                       const uint8_t* __restrict__ key_mask, const __nv_bfloat16* __restrict__ qg,
+                       const uint8_t* __restrict__ key_mask, int mrows, const __nv_bfloat16* __restrict__ qg,
                        const __nv_bfloat16* __restrict__ dog, __nv_bfloat16* __restrict__ dq, int B, int H,
                        int num_items, float scale, float scale_log2, DevCtx ctx) {
   using L = DqLayout<D>;
@@ -737,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < nkt; ++j) {
         uint32_t words[4] = {0u, 0u, 0u, 0u};
         if (kMask) {
-          key_tile_bits(mask, kd, w.b, j, words);
+          key_tile_bits(mask, kd, w.b % mrows, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
 #pragma unroll
@@ -747,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && use > 0) ok = wait_or_abort(&ctl->bar_kv_empty[slot], (use - 1) & 1, ctx, ctl);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
-          if (lane == 0) {
+          if (lane == 0 && (int)n != ctx.drop_load) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
             int ms = 0, row0 = j * kBT;
             if constexpr (kSeg) {
@@ -831,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the key tiles of this item, in order (all lanes evaluate the same mask)
       auto next_tile = [&](int from) {
         for (int jj = from; jj < nkt; ++jj)
-          if (!kMask || key_tile_any(mask, kd, w.b, jj)) return jj;
+          if (!kMask || key_tile_any(mask, kd, w.b % mrows, jj)) return jj;
         return nkt;
       };
       int j = next_tile(0);
@@ -934,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nkt; ++j) {
         uint32_t words[4];
         if (kMask) {
-          key_tile_bits(mask, kd, w.b, j, words);
+          key_tile_bits(mask, kd, w.b % mrows, j, words);
           if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
         // is there a next key tile?  Its K and V are read by the MMAs this tile's
@@ -943,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool has_next = j + 1 < nkt;
         if (kMask) {
           int jn = j + 1;
-          while (jn < nkt && !key_tile_any(mask, kd, w.b, jn)) ++jn;
+          while (jn < nkt && !key_tile_any(mask, kd, w.b % mrows, jn)) ++jn;
           has_next = jn < nkt;
         }
         if (has_next) {
@@ -1084,8 +1059,8 @@ int record_prof(int i, cudaStream_t stream) {
 
 template <int D, bool kMask>
 int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
-               const uint8_t* mask, void* dq, void* dk, void* dv, int B, const SeqDesc& qd, const SeqDesc& kd, int H,
-               float scale, float* delta, cudaStream_t stream, const DevCtx& ctx) {
+               const uint8_t* mask, int mrows, void* dq, void* dk, void* dv, int B, const SeqDesc& qd,
+               const SeqDesc& kd, int H, float scale, float* delta, cudaStream_t stream, const DevCtx& ctx) {
   const size_t rows = (size_t)B * qd.total * H;
   const int nqt = qd.tile0[qd.nseg], nkt = kd.tile0[kd.nseg];
   float* nl2 = delta + (size_t)B * H * nqt * kBT;
@@ -1111,7 +1086,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid_k, kThreads, smem, stream>>>(mq, mk, mv, mdo, qd, kd, nl2, delta, mask,
+    kern<<<grid_k, kThreads, smem, stream>>>(mq, mk, mv, mdo, qd, kd, nl2, delta, mask, mrows,
                                              static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), B, H,
                                              (int)items_k, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
@@ -1122,7 +1097,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DqLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid_q, kThreads, smem, stream>>>(mk, mv, qd, kd, nl2, delta, mask, static_cast<const __nv_bfloat16*>(q),
+    kern<<<grid_q, kThreads, smem, stream>>>(mk, mv, qd, kd, nl2, delta, mask, mrows,
+                                             static_cast<const __nv_bfloat16*>(q),
                                              static_cast<const __nv_bfloat16*>(dout), static_cast<__nv_bfloat16*>(dq),
                                              B, H, (int)items_q, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dQ)"))) return st;
@@ -1130,18 +1106,15 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
   return record_prof(2, stream);
 }
 
+// mrows: rows of key_mask; batch b uses row b % mrows
 int bwd_dispatch(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
-                 const uint8_t* key_mask, void* dq, void* dk, void* dv, int B, const SeqDesc& qd, const SeqDesc& kd,
-                 int H, int D, float scale, float* delta, cudaStream_t s, const DevCtx& ctx) {
-  if (D == 64)
-    return key_mask ? launch_bwd<64, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta, s,
-                                           ctx)
-                    : launch_bwd<64, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta,
-                                            s, ctx);
-  return key_mask ? launch_bwd<128, true>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta, s,
-                                          ctx)
-                  : launch_bwd<128, false>(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, qd, kd, H, scale, delta, s,
-                                           ctx);
+                 const uint8_t* key_mask, int mrows, void* dq, void* dk, void* dv, int B, const SeqDesc& qd,
+                 const SeqDesc& kd, int H, int D, float scale, float* delta, cudaStream_t s, const DevCtx& ctx) {
+#define UAA_BWD(DD, MM) \
+  launch_bwd<DD, MM>(q, k, v, out, dout, lse, key_mask, mrows, dq, dk, dv, B, qd, kd, H, scale, delta, s, ctx)
+  if (D == 64) return key_mask ? UAA_BWD(64, true) : UAA_BWD(64, false);
+  return key_mask ? UAA_BWD(128, true) : UAA_BWD(128, false);
+#undef UAA_BWD
 }
 
 }  // namespace
@@ -1183,8 +1156,8 @@ extern "C" int uaa_attn_bwd_cross(const void* q, const void* k, const void* v, c
     return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
   DevCtx ctx;
   if ((st = get_dev_ctx(&ctx))) return st;
-  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, seq_plain(Sq), seq_plain(Sk), H, D, scale,
-                      static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), ctx);
+  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, B, dq, dk, dv, B, seq_plain(Sq), seq_plain(Sk), H, D,
+                      scale, static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), ctx);
 }
 
 extern "C" size_t uaa_ulysses_attn_bwd_workspace_bytes(int P, const int* shard_lens, int cap, int B, int H, int D) {
@@ -1226,7 +1199,7 @@ extern "C" int uaa_ulysses_attn_bwd(const void* q, const void* k, const void* v,
     return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
   DevCtx ctx;
   if ((st = get_dev_ctx(&ctx))) return st;
-  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, sd, sd, H, D, scale,
+  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, B, dq, dk, dv, B, sd, sd, H, D, scale,
                       static_cast<float*>(workspace), s, ctx);
 }
 
@@ -1236,6 +1209,34 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
                             uaa_stream_t stream) {
   return uaa_attn_bwd_cross(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, S, H, D, scale, workspace,
                             workspace_bytes, stream);
+}
+
+extern "C" int uaa_attn_bwd_groups(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                   const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int G,
+                                   int B, int S, int H, int D, float scale, void* workspace, size_t workspace_bytes,
+                                   uaa_stream_t stream) {
+  const char* fn = "uaa_attn_bwd_groups";
+  if (G < 1 || B < 0) return set_error(UAA_ERR_INVALID_ARG, "%s: G=%d, B=%d", fn, G, B);
+  if ((long long)G * B > 65535) return set_error(UAA_ERR_UNSUPPORTED, "%s: G*B must be <= 65535", fn);
+  const int GB = G * B;
+  int st = validate_attn_sizes(fn, GB, S, S, H, D, scale);
+  if (st) return st;
+  if ((uint64_t)GB * S * H == 0) return UAA_OK;
+  if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
+      (st = check_dev_ptr(fn, "out", out)) || (st = check_dev_ptr(fn, "dout", dout)) ||
+      (st = check_dev_ptr(fn, "dq", dq)) || (st = check_dev_ptr(fn, "dk", dk)) || (st = check_dev_ptr(fn, "dv", dv)))
+    return st;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: lse is NULL or not 4-byte aligned", fn);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: workspace is NULL or not 256-byte aligned", fn);
+  const size_t need = uaa_attn_bwd_workspace_bytes(GB, S, H, D);
+  if (workspace_bytes < need)
+    return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
+  DevCtx ctx;
+  if ((st = get_dev_ctx(&ctx))) return st;
+  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, B, dq, dk, dv, GB, seq_plain(S), seq_plain(S), H, D, scale,
+                      static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), ctx);
 }
 
 // ---------------------------------------------------------------------------

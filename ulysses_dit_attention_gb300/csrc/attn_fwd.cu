@@ -57,6 +57,11 @@ constexpr float kRescaleThreshold = 8.0f;
 // arrive, the issuer warp syncs)
 constexpr uint32_t kBarP = 1;
 constexpr uint32_t kBarPCount = 128 + 32;  // log2 units: rescale O only when the max grows by > 2^8
+// With a key mask of at most this many rows, key tiles without an attended key
+// are skipped: their counts per mask row are tabulated in shared memory when the
+// kernel starts (above this many rows every tile is visited and masked keys only
+// get P = 0).
+constexpr int kMaxCntRows = 256;
 
 template <int D>
 struct FwdLayout {
@@ -65,7 +70,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;                                  // two Q tiles
   static constexpr int kRingOff = kQ + 2 * kTileBytes;          // K/V ring
   static constexpr int kCtl = kRingOff + kRing * kTileBytes;
-  static constexpr int kSmem = kCtl + 512;
+  static constexpr int kCnt = kCtl + 512;                       // attended key tiles per mask row
+  static constexpr int kSmem = kCnt + kMaxCntRows * 4;
   static_assert(kSmem <= 232448, "forward shared memory exceeds the per-CTA limit");
   static_assert(kRing <= 5, "control block holds five ring slots");
 };
@@ -96,31 +102,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const DevCtx& ctx, FwdCtl* ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-    if (*reinterpret_cast<volatile unsigned int*>(ctx.status) & kStatusTimeout) {
-      // another CTA already gave up: stop waiting (the launch has failed)
-      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-      return false;
-    }
-    if (globaltimer_ns() - t0 > ctx.timeout_ns) {
-      atomicOr(ctx.status, kStatusTimeout);
-      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-      return false;
-    }
-  }
-}
-
-// Bounded wait used during teardown: does not give up on the abort flag.
-__device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity, const DevCtx& ctx) {
-  if (!mbar_wait(bar, parity, ctx.timeout_ns)) atomicOr(ctx.status, kStatusTimeout);
-}
 
 struct Item {
   int qp, h, b;
@@ -142,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ SegMaps tmQ, const __grid_constant__ SegMaps tmK,
                     const __grid_constant__ SegMaps tmV, const __grid_constant__ SeqDesc qd,
                     const __grid_constant__ SeqDesc kd,
-                    const uint8_t* __restrict__ key_mask, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                    int B, int H, int num_items, float scale_log2, DevCtx ctx) {
+                    const uint8_t* __restrict__ key_mask, int mrows, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse, int B, int H, int num_items, float scale_log2, DevCtx ctx) {
   using L = FwdLayout<D>;
   constexpr int kChunks = D / 64;
   constexpr int R = L::kRing;
@@ -193,10 +174,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem_base, 512);
     tmem_relinquish();
   }
+  // Key tiles with at least one attended key, per mask row (batch b uses row b % mrows).
+  // Every role takes its per-item tile count from this table, which no one writes after
+  // the start, so producer, issuer and softmax walk the same schedule -- after a failure
+  // too (the forward's named barriers rely on it).
+  int* tile_cnt = reinterpret_cast<int*>(smem + L::kCnt);
+  const bool skip = kMask && mrows <= kMaxCntRows;
+  if (skip) {
+    for (int r = threadIdx.x; r < mrows; r += kThreads) tile_cnt[r] = 0;
+    __syncthreads();
+    // one warp per (row, tile) pair, four tiles in flight per warp
+    const int pairs = mrows * nkt;
+    for (int p0 = warp * 4; p0 < pairs; p0 += (kThreads / 32) * 4) {
+      bool any[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pr = p0 + u;
+        bool hit = false;
+        if (pr < pairs) {
+          const int r = pr / nkt, j = pr - r * nkt;
+          const SeqTile kt = seq_tile(kd, j);
+          const uint8_t* row = key_mask + (size_t)r * Sk + kd.off[kt.seg] + kt.row0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = 32 * t + lane;
+            hit |= c < kt.valid && row[c] != 0;
+          }
+        }
+        any[u] = hit;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (__any_sync(0xffffffffu, any[u]) && lane == 0 && p0 + u < pairs) atomicAdd(&tile_cnt[(p0 + u) / nkt], 1);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  // key tiles an item of batch b walks
+  auto item_tiles = [&](int b) { return skip ? tile_cnt[b % mrows] : nkt; };
 
   // Teardown bookkeeping of the producer: uses armed per barrier.
   uint32_t kv_armed[5] = {0, 0, 0, 0, 0};
@@ -206,12 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    uint32_t n = 0;  // K/V ring counter across items
-    uint32_t it = 0;
-    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
+    uint32_t n = 0;   // K/V ring counter across items
+    uint32_t ne = 0;  // items with at least one attended key tile (the Q buffer's uses)
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item w = decode_item(item, nqp, H);
+      if (item_tiles(w.b) == 0) continue;  // no attended key: the softmax warps write O = 0
+      const int mb = w.b % mrows;
       if (lane == 0) {
-        if (it > 0) ok = wait_or_abort(&ctl->bar_q_empty, (it - 1) & 1, ctx, ctl);
+        if (ne > 0) ok = wait_or_abort(&ctl->bar_q_empty, (ne - 1) & 1, ctx, ctl);
         if (ok) {
           mbar_arrive_expect_tx(&ctl->bar_q_full, 2 * L::kTileBytes);
 #pragma unroll
@@ -223,10 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(smem + L::kQ + t * L::kTileBytes + c * kChunkBytes, &tmQ.m[qt.seg], &ctl->bar_q_full,
                           c * 64, w.h, qt.row0, w.b);
           }
-          q_armed = it + 1;
+          q_armed = ne + 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++ne;
       SeqCursor kseg;  // key segment cursor (tiles are visited in order)
       for (int j = 0; ok && j < nkt; ++j) {
         SeqTile kt;
@@ -237,6 +257,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           kt.row0 = j * kBN;
           kt.valid = Sk - kt.row0 < kBN ? Sk - kt.row0 : kBN;
         }
+        // bit c of word t: key c' = 32t + c of the tile (sequence position off + row0 + c')
+        // exists and is attended
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
+        if (kMask) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = 32 * t + lane;
+            const bool valid = c < kt.valid && key_mask[(size_t)mb * Sk + kd.off[kt.seg] + kt.row0 + c] != 0;
+            words[t] = __ballot_sync(0xffffffffu, valid);
+          }
+          // the same test as the tile-count table: the softmax and issuer expect exactly those tiles
+          if (skip && (words[0] | words[1] | words[2] | words[3]) == 0) continue;
+        }
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
           const int slot = n % R;
@@ -244,23 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && use > 0) ok = wait_or_abort(&ctl->bar_kv_empty[slot], (use - 1) & 1, ctx, ctl);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
-          if (kMask && kind == 1) {
-            // bit c of word t: key c' = 32t + c of the tile (sequence position
-            // off + row0 + c') exists and is attended
-            uint32_t words[4];
+          if (kMask && kind == 1 && lane == 0) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int c = 32 * t + lane;
-              const bool valid = c < kt.valid && key_mask[(size_t)w.b * Sk + kd.off[kt.seg] + kt.row0 + c] != 0;
-              words[t] = __ballot_sync(0xffffffffu, valid);
-            }
-            if (lane == 0) {
-#pragma unroll
-              for (int t = 0; t < 4; ++t) ctl->mask_words[slot][t] = words[t];
-            }
-            __syncwarp();
+            for (int t = 0; t < 4; ++t) ctl->mask_words[slot][t] = words[t];
           }
-          if (lane == 0) {
+          if (lane == 0 && (int)n != ctx.drop_load) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
             const int ms = kSeg ? kt.seg : 0;
             const CUtensorMap* map = kind == 0 ? &tmK.m[ms] : &tmV.m[ms];
@@ -281,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warpgroup of tile t arrives on.
     const bool leader = lane == 0;
     bool ok = true;
-    uint32_t g = 0;  // global tile counter across items (phase index of s/pv barriers)
-    uint32_t it = 0;
+    uint32_t g = 0;   // global tile counter across items (phase index of s/pv barriers)
+    uint32_t ne = 0;  // items with at least one attended key tile (phases of q_full, o_free)
     auto ring_addr = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
     auto issue_s = [&](int t, uint32_t nk) {
       const uint32_t sQ = sbase + L::kQ + t * L::kTileBytes;
@@ -306,7 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_ts(d, aP + kk * 8, desc_add(dv0, kk * 2048), kIdescPV, (acc || kk > 0) ? 1u : 0u);
       mma_commit(&ctl->bar_pv_done[t]);
     };
-    for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++it) {
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+      // an item without an attended key tile takes no MMA and no barrier
+      const int nt = item_tiles(decode_item(item, nqp, H).b);
+      if (nt == 0) continue;
       // After a failure anywhere in the CTA this warp stops issuing but still
       // meets the softmax warpgroups at every named barrier of the schedule.
       if (ok && *reinterpret_cast<volatile int*>(&ctl->abort)) ok = false;
@@ -314,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         bool w = true;
         if (leader) {
-          w = wait_or_abort(&ctl->bar_q_full, it & 1, ctx, ctl);
+          w = wait_or_abort(&ctl->bar_q_full, ne & 1, ctx, ctl);
           if (w) w = wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl);
           if (w) {
             tc_fence_after();
@@ -326,18 +350,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, w, 0);
       }
-      for (int j = 0; j < nkt; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const uint32_t gj = g + j;
         const uint32_t nv = 2 * gj + 1;
-        const bool more = j + 1 < nkt;
+        const bool more = j + 1 < nt;
         const uint32_t nk1 = 2 * (gj + 1);
         // tile 0: PV0_j, then S0_{j+1}.  V_j and K_{j+1} have landed: the softmax
         // warpgroups wait for them before they arrive.
         named_sync(kBarP + 0, kBarPCount);
-        if (ok && j == 0 && it > 0) {
+        if (ok && j == 0 && ne > 0) {
           // the previous item's epilogue must have read O before PV0_0 overwrites it
           bool w = true;
-          if (leader) w = wait_or_abort(&ctl->bar_o_free, (it - 1) & 1, ctx, ctl);
+          if (leader) w = wait_or_abort(&ctl->bar_o_free, (ne - 1) & 1, ctx, ctl);
           ok = __shfl_sync(0xffffffffu, w, 0);
         }
         if (ok && leader) {
@@ -362,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // both Q tiles are free once this item's MMAs are done
       if (ok && leader) mma_commit(&ctl->bar_q_empty);
       __syncwarp();
-      g += nkt;
+      g += nt;
+      ++ne;
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -373,13 +398,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t colO = 256 + (uint32_t)(t * D);
     bool ok = true;
     uint32_t g = 0;
-    uint32_t it = 0;
-    for (int item = blockIdx.x; item < num_items; item += gridDim.x, ++it) {
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
       const Item w = decode_item(item, nqp, H);
+      const int nt = item_tiles(w.b);
+      if (nt == 0) {
+        // no attended key for this batch: O = 0 and LSE = -inf, without MMAs or barriers
+        const SeqTile qt = seq_tile(qd, 2 * w.qp + t);
+        if (row < qt.valid) {
+          const int qs = qt.row0 + row;
+          __nv_bfloat16* orow = out + seq_elem(qd, B, H, D, w.b, qt.seg, qs, w.h);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+          lse[((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs] = -INFINITY;
+        }
+        continue;
+      }
       float mu = -INFINITY;  // log2-domain offset in use (scaled max, possibly stale by < 2^8)
       float l_run = 0.f;
       SeqCursor kseg;  // key segment cursor
-      for (int j = 0; j < nkt; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const uint32_t gj = g + j;
         if (ok) {
           // V_j and K_{j+1}, read by the MMAs that this step's arrival releases,
@@ -387,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // these waits off both the issuing thread and the S -> P path
           const uint32_t nv = 2 * gj + 1, nk1 = nv + 1;
           bool okw = wait_or_abort(&ctl->bar_kv_full[nv % R], (nv / R) & 1, ctx, ctl);
-          if (okw && j + 1 < nkt) okw = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl);
+          if (okw && j + 1 < nt) okw = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl);
           if (okw) okw = wait_or_abort(&ctl->bar_s_full[t], gj & 1, ctx, ctl);
           ok = __all_sync(0xffffffffu, okw);
         }
@@ -471,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         named_arrive(kBarP + t, kBarPCount);
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (g + nkt - 1) & 1, ctx, ctl));
+      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_pv_done[t], (g + nt - 1) & 1, ctx, ctl));
       if (!ok) {
-        g += nkt;
+        g += nt;
         continue;
       }
       tc_fence_after();
@@ -502,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&ctl->bar_o_free);
       if (qvalid)
         lse[((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
-      g += nkt;
+      g += nt;
     }
   }
 
@@ -539,8 +576,9 @@ int sm_count() {
 }
 
 template <int D, bool kMask, bool kSeg>
-int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, void* out, float* lse, int B,
-               const SeqDesc& qd, const SeqDesc& kd, int H, float scale, cudaStream_t stream, const DevCtx& ctx) {
+int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, int mrows, void* out, float* lse,
+               int B, const SeqDesc& qd, const SeqDesc& kd, int H, float scale, cudaStream_t stream,
+               const DevCtx& ctx) {
   SegMaps mq, mk, mv;
   int st;
   if ((st = encode_seq_maps(&mq, q, qd, B, H, D, 128))) return st;
@@ -554,15 +592,18 @@ int launch_fwd(const void* q, const void* k, const void* v, const uint8_t* mask,
   const long long items = nqp * H * B;
   if (items > INT32_MAX) return set_error(UAA_ERR_UNSUPPORTED, "uaa_attn_fwd: too many work items");
   const int grid = (int)(items < sm_count() ? items : sm_count());
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, qd, kd, mask, static_cast<__nv_bfloat16*>(out), lse, B, H,
-                                         (int)items, scale * kLog2e, ctx);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, qd, kd, mask, mrows, static_cast<__nv_bfloat16*>(out), lse, B,
+                                         H, (int)items, scale * kLog2e, ctx);
   return check_launch("uaa_attn_fwd");
 }
 
-int fwd_dispatch(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out, float* lse, int B,
-                 const SeqDesc& qd, const SeqDesc& kd, int H, int D, float scale, cudaStream_t s, const DevCtx& ctx) {
+// mrows: rows of key_mask; batch b uses row b % mrows (mrows = B, or the B batches shared by
+// the G head groups of a Ulysses step launched as one batch of G*B)
+int fwd_dispatch(const void* q, const void* k, const void* v, const uint8_t* key_mask, int mrows, void* out,
+                 float* lse, int B, const SeqDesc& qd, const SeqDesc& kd, int H, int D, float scale, cudaStream_t s,
+                 const DevCtx& ctx) {
   const bool seg = qd.nseg > 1 || kd.nseg > 1;
-#define UAA_FWD(DD, MM, SS) launch_fwd<DD, MM, SS>(q, k, v, key_mask, out, lse, B, qd, kd, H, scale, s, ctx)
+#define UAA_FWD(DD, MM, SS) launch_fwd<DD, MM, SS>(q, k, v, key_mask, mrows, out, lse, B, qd, kd, H, scale, s, ctx)
   if (D == 64) {
     if (seg) return key_mask ? UAA_FWD(64, true, true) : UAA_FWD(64, false, true);
     return key_mask ? UAA_FWD(64, true, false) : UAA_FWD(64, false, false);
@@ -612,13 +653,32 @@ extern "C" int uaa_attn_fwd_cross(const void* q, const void* k, const void* v, c
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return set_error(UAA_ERR_INVALID_ARG, "%s: lse is not 4-byte aligned", fn);
   DevCtx ctx;
   if ((st = get_dev_ctx(&ctx))) return st;
-  return fwd_dispatch(q, k, v, key_mask, out, lse, B, seq_plain(Sq), seq_plain(Sk), H, D, scale,
+  return fwd_dispatch(q, k, v, key_mask, B, out, lse, B, seq_plain(Sq), seq_plain(Sk), H, D, scale,
                       static_cast<cudaStream_t>(stream), ctx);
 }
 
 extern "C" int uaa_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
                             float* lse, int B, int S, int H, int D, float scale, uaa_stream_t stream) {
   return uaa_attn_fwd_cross(q, k, v, key_mask, out, lse, B, S, S, H, D, scale, stream);
+}
+
+extern "C" int uaa_attn_fwd_groups(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
+                                   float* lse, int G, int B, int S, int H, int D, float scale, uaa_stream_t stream) {
+  const char* fn = "uaa_attn_fwd_groups";
+  if (G < 1 || B < 0) return set_error(UAA_ERR_INVALID_ARG, "%s: G=%d, B=%d", fn, G, B);
+  if ((long long)G * B > 65535) return set_error(UAA_ERR_UNSUPPORTED, "%s: G*B must be <= 65535", fn);
+  int st = validate_attn_sizes(fn, G * B, S, S, H, D, scale);
+  if (st) return st;
+  if ((uint64_t)B * S * H == 0) return UAA_OK;
+  if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
+      (st = check_dev_ptr(fn, "out", out)))
+    return st;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: lse is NULL or not 4-byte aligned", fn);
+  DevCtx ctx;
+  if ((st = get_dev_ctx(&ctx))) return st;
+  return fwd_dispatch(q, k, v, key_mask, B, out, lse, G * B, seq_plain(S), seq_plain(S), H, D, scale,
+                      static_cast<cudaStream_t>(stream), ctx);
 }
 
 extern "C" int uaa_ulysses_attn_fwd(const void* q, const void* k, const void* v, const uint8_t* key_mask, void* out,
@@ -643,5 +703,5 @@ extern "C" int uaa_ulysses_attn_fwd(const void* q, const void* k, const void* v,
   // padding rows of the output shards are zero, as after the head->seq exchange
   if ((st = zero_pad_rows(out, sd, B, H, D, s))) return st;
   if (sd.total == 0) return UAA_OK;
-  return fwd_dispatch(q, k, v, key_mask, out, lse, B, sd, sd, H, D, scale, s, ctx);
+  return fwd_dispatch(q, k, v, key_mask, B, out, lse, B, sd, sd, H, D, scale, s, ctx);
 }

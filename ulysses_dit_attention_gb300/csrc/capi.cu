@@ -15,15 +15,21 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
-// The status word: one per device, a file-scope device variable of this
-// translation unit.  Its device address is looked up once per device.
-__device__ unsigned int g_status_word;
+// The status words: one pair per device (sticky status bits, epoch of the last
+// call that gave up), a file-scope device variable of this translation unit.
+// Its device address is looked up once per device.
+__device__ unsigned int g_status_word[2];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 unsigned int* g_status_addr[kMaxDevices] = {nullptr};
 
-std::atomic<unsigned long long> g_timeout_ns{4000ull * 1000ull * 1000ull};
+constexpr unsigned long long kDefaultTimeoutNs = 4000ull * 1000ull * 1000ull;
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+// Call epochs: every get_dev_ctx() (one per C-ABI call) takes the next one; 0 is never used.
+std::atomic<unsigned int> g_epoch{0};
+// Diagnostic: the ring load that the attention kernels' producers skip (-1: none).
+std::atomic<int> g_drop_load{-1};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -61,6 +67,12 @@ int get_dev_ctx(DevCtx* ctx) {
     ctx->status = g_status_addr[dev];
   }
   ctx->timeout_ns = g_timeout_ns.load();
+  // teardown waits only wait for copies and MMAs already issued: never shorter than the default
+  ctx->settle_ns = ctx->timeout_ns > kDefaultTimeoutNs ? ctx->timeout_ns : kDefaultTimeoutNs;
+  unsigned int ep = ++g_epoch;
+  if (ep == 0) ep = ++g_epoch;
+  ctx->epoch = ep;
+  ctx->drop_load = g_drop_load.load();
   return UAA_OK;
 }
 
@@ -156,9 +168,10 @@ const char* uaa_last_error(void) { return g_last_error; }
 const char* uaa_version(void) { return "uaa 0.1 sm_103a"; }
 
 void uaa_set_wait_timeout_ms(unsigned int ms) {
-  unsigned long long v = ms ? (unsigned long long)ms : 4000ull;
-  g_timeout_ns.store(v * 1000ull * 1000ull);
+  g_timeout_ns.store(ms ? (unsigned long long)ms * 1000ull * 1000ull : kDefaultTimeoutNs);
 }
+
+void uaa_debug_drop_load(int n) { g_drop_load.store(n < 0 ? -1 : n); }
 
 int uaa_check_device_status(uaa_stream_t stream) {
   DevCtx ctx;
@@ -167,7 +180,7 @@ int uaa_check_device_status(uaa_stream_t stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
-  unsigned int word = 0;
+  unsigned int word = 0;  // the sticky bits; the abort epoch needs no clearing (an epoch recurs only after 2^32 calls)
   e = cudaMemcpy(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   if (word) {

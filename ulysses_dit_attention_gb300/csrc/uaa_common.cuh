@@ -23,9 +23,18 @@ enum : uint32_t {
   kStatusBadLaunch = 2u,    // a kernel refused its launch configuration (e.g. misaligned shared memory)
 };
 
+// Launch context handed to every kernel.  status[0] holds the sticky status
+// bits above (reported and cleared by uaa_check_device_status); status[1] holds
+// the epoch of the last call whose kernels gave up.  Every C-ABI call gets a new
+// epoch, so a timeout makes the other CTAs and kernels of the same call stop
+// waiting, while later calls -- whose epochs differ -- run normally even before
+// the status has been read.
 struct DevCtx {
-  unsigned int* status;     // device status word of the current device
-  unsigned long long timeout_ns;
+  unsigned int* status;           // two words of the current device: status bits, abort epoch
+  unsigned long long timeout_ns;  // bound of every wait for another role's progress
+  unsigned long long settle_ns;   // bound of the teardown waits for copies / MMAs already in flight
+  unsigned int epoch;             // this call's epoch (never 0)
+  int drop_load;                  // diagnostic: the ring load each producer skips (-1: none)
 };
 
 // Host side: per-device status word address, wait bound, error message.
@@ -128,6 +137,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
+}
+
+// Bounded wait of a kernel role on barrier phase `parity`.  Returns false --
+// and the role then leaves its loops -- when the phase did not complete within
+// ctx.timeout_ns (the device status records a timeout and this call's epoch is
+// published so that every CTA of the call stops waiting), when another role of
+// this CTA has already given up (ctl->abort), or when another CTA of the same
+// call has (status[1] == epoch).
+template <typename Ctl>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const DevCtx& ctx, Ctl* ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+    if (reinterpret_cast<volatile unsigned int*>(ctx.status)[1] == ctx.epoch) {
+      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > ctx.timeout_ns) {
+      atomicOr(ctx.status, kStatusTimeout);
+      atomicExch(ctx.status + 1, ctx.epoch);
+      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+      return false;
+    }
+  }
+}
+
+// Teardown wait for work that is already in flight (a TMA copy into this CTA's
+// shared memory, the last MMAs before TMEM is released): it ignores the abort
+// flags, which only stop waits for other roles, and has its own, longer bound.
+__device__ __forceinline__ void settle(uint64_t* bar, uint32_t parity, const DevCtx& ctx) {
+  if (!mbar_wait(bar, parity, ctx.settle_ns)) atomicOr(ctx.status, kStatusTimeout);
 }
 
 // ---------------------------------------------------------------- TMA
