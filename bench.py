@@ -254,7 +254,7 @@ PER_CONFIG = ("layout_b2_s16_h16_d64", "dit_b2_s1024_h24_d64", "mask_b4_s4096_h2
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 
 
-def time_config(uaa, w, dev, warmup, iters):
+def time_config(uaa, w, dev, warmup, iters, fused_bwd=False):
     """fwd, bwd and fwd+bwd of one workload through the C ABI, each captured once in a CUDA graph
     and replayed: CUDA events around every replay, the L2 flushed (a 256 MB write) between replays
     when the inputs fit in L2, median over ``iters`` replays; plus the backward's per-kernel split
@@ -265,7 +265,8 @@ def time_config(uaa, w, dev, warmup, iters):
     mask = None if inp["mask"] is None else inp["mask"].to(dev)
     out, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(1, uaa.attn_bwd_workspace_bytes(B, S, H, D)), dtype=torch.uint8, device=dev)
+    ws_fn = uaa.attn_bwd_fused_workspace_bytes if fused_bwd else uaa.attn_bwd_workspace_bytes
+    ws = torch.empty(max(1, ws_fn(B, S, H, D)), dtype=torch.uint8, device=dev)
     in_bytes = 4 * q.numel() * q.element_size()
     flush = in_bytes < 2 * (129 << 20)
     scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
@@ -274,7 +275,7 @@ def time_config(uaa, w, dev, warmup, iters):
         uaa.attn_fwd(q, k, v, mask, w.scale, out=out, lse=lse)
 
     def bwd():
-        uaa.attn_bwd(q, k, v, out, do, lse, mask, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        uaa.attn_bwd(q, k, v, out, do, lse, mask, w.scale, dq=dq, dk=dk, dv=dv, workspace=ws, fused=fused_bwd)
 
     def both():
         fwd()
@@ -331,13 +332,30 @@ def time_config(uaa, w, dev, warmup, iters):
            "fwd_ms": ms["fwd"], "bwd_ms": ms["bwd"], "fwd_bwd_ms": ms["fwd_bwd"],
            "fwd_tflops": ffl / (ms["fwd"] * 1e-3) / 1e12, "bwd_tflops": bfl / (ms["bwd"] * 1e-3) / 1e12,
            "fwd_bwd_tflops": (ffl + bfl) / (ms["fwd_bwd"] * 1e-3) / 1e12,
-           "bwd_kernels_ms": {"attn_bwd_dkdv_kernel": dkdv_ms, "attn_bwd_dq_kernel": dq_ms},
+           "bwd_kernels_ms": ({"attn_bwd_fused_kernel": dkdv_ms, "dq_convert_kernel": dq_ms} if fused_bwd else
+                              {"attn_bwd_dkdv_kernel": dkdv_ms, "attn_bwd_dq_kernel": dq_ms}),
+           "bwd": "one pass, dQ by fp32 reductions" if fused_bwd else "split dK/dV and dQ passes",
            "timing": (f"CUDA graph replays, median of {iters}, "
                       + ("L2 flushed (256 MB write) before each replay" if flush else
                          "inputs larger than L2, no flush"))}
     del q, k, v, do, out, dq, dk, dv, lse, ws, scratch
     torch.cuda.empty_cache()
     return rec
+
+
+def run_one_workload(args, local):
+    """``--workload NAME``: the per-workload record of one workload alone (used for profiling)."""
+    import ulysses_dit_attention_gb300 as uaa
+    from ulysses_dit_attention_gb300 import build as uaa_build
+
+    uaa_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.workload(args.workload)
+    big = w.S * w.S * w.H * w.B > (1 << 32)
+    rec = time_config(uaa, w, dev, warmup=args.warmup, iters=args.steps if big else max(args.steps, 10),
+                      fused_bwd=args.bwd == "fused")
+    print(json.dumps({"workload": w.name, **rec}))
 
 
 def run_configs(uaa, args, dev, local):
@@ -351,7 +369,8 @@ def run_configs(uaa, args, dev, local):
         for name in PER_CONFIG:
             w = synth.workload(name)
             big = w.S * w.S * w.H * w.B > (1 << 32)
-            recs[name] = time_config(uaa, w, dev, warmup=3 if big else 10, iters=5 if big else 30)
+            recs[name] = time_config(uaa, w, dev, warmup=3 if big else 10, iters=5 if big else 30,
+                                     fused_bwd=args.bwd == "fused")
     for name in PER_CONFIG:
         w = synth.workload(name)
         r = recs[name]
@@ -415,7 +434,9 @@ def run_gpu(args, world, rank, local):
     yo, ydq, ydk, ydv = (torch.empty_like(yq) for _ in range(4))
     lse = torch.empty((P, B, Hg, S), dtype=torch.float32, device=dev)
     o_sh, dq_sh, dk_sh, dv_sh = (torch.empty_like(sh["q"]) for _ in range(4))
-    ws = torch.empty(uaa.attn_bwd_workspace_bytes(P * B, S, Hg, D), dtype=torch.uint8, device=dev)
+    fused_bwd = args.bwd == "fused"
+    ws_bytes = (uaa.attn_bwd_fused_workspace_bytes if fused_bwd else uaa.attn_bwd_workspace_bytes)(P * B, S, Hg, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     fused = args.path == "fused"
     if fused:
         # the exchanges fused into the attention kernels: the step reads and writes the shards only
@@ -478,7 +499,7 @@ def run_gpu(args, world, rank, local):
             uaa.set_bwd_profile_events(next(prof_iter))
         g4 = lambda t: t.view(P * B, S, Hg, D)  # noqa: E731
         uaa.attn_bwd(g4(yq), g4(yk), g4(yv), g4(yo), g4(ydo), lse.view(P * B, Hg, S), None, w.scale, dq=g4(ydq),
-                     dk=g4(ydk), dv=g4(ydv), workspace=ws)
+                     dk=g4(ydk), dv=g4(ydv), workspace=ws, fused=fused_bwd)
         if timed:
             uaa.set_bwd_profile_events(None)
             mark("bwd1")
@@ -566,7 +587,7 @@ def run_gpu(args, world, rank, local):
         e_do_free.record(stream)
         g4 = lambda t: t.view(P * B, S, Hg, D)  # noqa: E731
         uaa.attn_bwd(g4(yq), g4(yk), g4(yv), g4(yo), g4(ydo), lse.view(P * B, Hg, S), None, w.scale, dq=g4(ydq),
-                     dk=g4(ydk), dv=g4(ydv), workspace=ws)
+                     dk=g4(ydk), dv=g4(ydv), workspace=ws, fused=fused_bwd)
         stream.wait_event(e_g_out)  # the previous step's read-back of the gradients is done
         for y, x in ((ydq, dq_sh), (ydk, dk_sh), (ydv, dv_sh)):
             uaa.head_to_seq(y, lens, cap, out=x)
@@ -648,12 +669,14 @@ def run_gpu(args, world, rank, local):
     peak_hbm, _ = _peak_value(pk, "hbm_gbs")
     dkdv_ms = sum(a.elapsed_time(b) for a, b, _ in prof) / len(prof)
     dq_ms = sum(b.elapsed_time(c) for _, b, c in prof) / len(prof)
-    # dK/dV kernel: the S, dP, dV and dK GEMMs of all P head groups = 8*P*B*Hg*S^2*D algorithmic FLOPs
-    dkdv_flops = 8 * P * B * Hg * S * S * D
+    # dominant kernel: the split dK/dV kernel (S, dP, dV, dK GEMMs of all P head groups = 8*P*B*Hg*S^2*D
+    # algorithmic FLOPs) or the one-pass backward kernel (the same plus dQ: 10*P*B*Hg*S^2*D)
+    dkdv_flops = (10 if fused_bwd else 8) * P * B * Hg * S * S * D
     achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "traffic": dkdv_traffic(),
-                "kernel": "attn_bwd_dkdv_kernel<128,false> (all head groups: S, dP, dV, dK GEMMs)",
+                "frac": achieved / peak_tf, "traffic": None if fused_bwd else dkdv_traffic(),
+                "kernel": ("attn_bwd_fused_kernel<128,false> (all head groups: S, dP, dV, dK, dQ GEMMs)" if fused_bwd
+                           else "attn_bwd_dkdv_kernel<128,false> (all head groups: S, dP, dV, dK GEMMs)"),
                 "flops_per_launch": dkdv_flops, "ms_per_launch": dkdv_ms,
                 "peak_source": f"{src} {key}"}
     cpu = None
@@ -668,14 +691,17 @@ def run_gpu(args, world, rank, local):
                    "cap": cap, "mask": None, "l2": "inputs larger than L2 (4 x 279 MB shards), no flush",
                    "path": "exchanges fused into the attention kernels" if fused else
                    "seq->head / head->seq re-layout kernels around the attention kernels",
+                   "bwd": "one pass, dQ by fp32 reductions" if fused_bwd else "split dK/dV and dQ passes",
                    "parallelism": "replicas" if world > 1 else "single GPU, 4 emulated Ulysses ranks"},
         "parts_ms_per_step": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms, "relayout": relayout_ms},
         "attn_fwd_tflops": flops(B, S, H, D, bwd=False) / (fwd_ms * 1e-3) / 1e12,
         "attn_bwd_tflops": flops(B, S, H, D, fwd=False) / (bwd_ms * 1e-3) / 1e12,
         "fwd_launch_tflops": flops(P * B, S, Hg, D, bwd=False) / (fwd_launch * 1e-3) / 1e12,
-        "kernel_ms_per_launch": {"attn_fwd_kernel": fwd_launch, "attn_bwd_dkdv_kernel": dkdv_ms,
-                                 "attn_bwd_dq_kernel": dq_ms},
-        "dq_kernel_tflops": (6 * P * B * Hg * S * S * D) / (dq_ms * 1e-3) / 1e12,
+        "kernel_ms_per_launch": ({"attn_fwd_kernel": fwd_launch, "attn_bwd_fused_kernel": dkdv_ms,
+                                  "dq_convert_kernel": dq_ms} if fused_bwd else
+                                 {"attn_fwd_kernel": fwd_launch, "attn_bwd_dkdv_kernel": dkdv_ms,
+                                  "attn_bwd_dq_kernel": dq_ms}),
+        "dq_kernel_tflops": None if fused_bwd else (6 * P * B * Hg * S * S * D) / (dq_ms * 1e-3) / 1e12,
         "relayout_gbs": relayout_bytes / (relayout_ms * 1e-3) / 1e9 if relayout_ms > 0 else None,
         "relayout_hbm_frac": ((relayout_bytes / (relayout_ms * 1e-3) / 1e9) / peak_hbm
                               if peak_hbm and relayout_ms > 0 else None),
@@ -703,6 +729,10 @@ def main():
     ap.add_argument("--cpu-config-seconds", type=float, default=30.0,
                     help="host-time budget of the oracle per workload record (0: skip)")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling-size variant)")
+    ap.add_argument("--bwd", default="split", choices=["split", "fused"],
+                    help="backward: split dK/dV + dQ passes (bit-reproducible) or one pass with dQ reductions")
+    ap.add_argument("--workload", default=None, choices=[w.name for w in synth.WORKLOADS],
+                    help="time only this workload's fwd / bwd / fwd+bwd record (no headline line)")
     ap.add_argument("--path", default="exchange", choices=["fused", "exchange"],
                     help="Ulysses step: attention kernels reading the shards directly, or separate re-layouts")
     args = ap.parse_args()
@@ -713,7 +743,10 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup(args.gpus)
-    run_gpu(args, world, rank, local)
+    if args.workload:
+        run_one_workload(args, local)
+    else:
+        run_gpu(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -131,6 +131,30 @@ int uaa_attn_bwd_cross(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int Sq, int Sk, int H, int D,
                        float scale, void* workspace, size_t workspace_bytes, uaa_stream_t stream);
 
+/* Workspace of uaa_attn_bwd_fused: the two fp32 row vectors of
+ * uaa_attn_bwd_workspace_bytes() followed by an fp32 (B, H, S_pad, D) dQ
+ * accumulator (S_pad = S rounded up to 128), rounded up to 256 bytes.
+ * Returns 0 for invalid sizes. */
+size_t uaa_attn_bwd_fused_workspace_bytes(int B, int S, int H, int D);
+
+/* Attention backward in one K/V-tile-major pass: same arguments and results
+ * as uaa_attn_bwd, but each (query tile, key tile) pair's dQ contribution dS K
+ * is a fifth GEMM of the same kernel, added into an fp32 dQ accumulator with
+ * vector reductions (red.global.add) and converted to bf16 at the end -- the
+ * five GEMMs of the gradient are each done once, where uaa_attn_bwd recomputes
+ * S and dP in a separate dQ pass (seven GEMMs).  The order of the dQ additions
+ * varies from run to run, so dQ is not bit-for-bit reproducible (dK and dV
+ * are); use uaa_attn_bwd where reproducible gradients are required.
+ * "double-transpose", description (the backward op contract); the pages leave
+ * open how dQ is formed.
+ *   workspace : at least uaa_attn_bwd_fused_workspace_bytes(B, S, H, D) bytes,
+ *               256-byte aligned; contents on entry are ignored
+ * Returns UAA_OK or a negative uaa_status. */
+int uaa_attn_bwd_fused(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, const uint8_t* key_mask,
+                       void* dq, void* dk, void* dv, int B, int S, int H, int D, float scale,
+                       void* workspace, size_t workspace_bytes, uaa_stream_t stream);
+
 /* Attention of the G head groups of one Ulysses step, launched together.
  * "UAA-bwd", What does this PR do: after the seq->head exchange every rank runs
  * the plain attention on its head group with the full key-padding mask; on one

@@ -24,7 +24,7 @@ import torch
 from .build import LIB_PATH
 
 __all__ = [
-    "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "seq_to_head", "head_to_seq",
+    "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_fused_workspace_bytes", "seq_to_head", "head_to_seq",
     "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms", "debug_drop_load",
     "set_bwd_profile_events", "Attention", "attn_fwd_groups", "attn_bwd_groups",
     "attention", "UlyssesAttention", "ulysses_attention", "STATUS",
@@ -52,6 +52,9 @@ _SIGS = {
     "uaa_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P,
                           ctypes.c_size_t, _P]),
     "uaa_attn_bwd_cross": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P,
+                                ctypes.c_size_t, _P]),
+    "uaa_attn_bwd_fused_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "uaa_attn_bwd_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P,
                                 ctypes.c_size_t, _P]),
     "uaa_attn_fwd_groups": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "uaa_attn_bwd_groups": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P,
@@ -185,10 +188,18 @@ def attn_bwd_workspace_bytes(B, S, H, D) -> int:
     return int(lib().uaa_attn_bwd_workspace_bytes(B, S, H, D))
 
 
-def attn_bwd(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=None, dv=None, workspace=None):
+def attn_bwd_fused_workspace_bytes(B, S, H, D) -> int:
+    return int(lib().uaa_attn_bwd_fused_workspace_bytes(B, S, H, D))
+
+
+def attn_bwd(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=None, dv=None, workspace=None,
+             fused=False):
     """``uaa_attn_bwd`` / ``uaa_attn_bwd_cross``: returns ``(dq, dk, dv)`` in bf16 BSHD.
 
-    ``k``, ``v`` (and ``dk``, ``dv``) may have another sequence length than ``q``.
+    ``k``, ``v`` (and ``dk``, ``dv``) may have another sequence length than ``q``.  With
+    ``fused=True`` (same sequence lengths only) the one-pass ``uaa_attn_bwd_fused`` runs
+    instead: five GEMMs instead of seven, dQ by fp32 reductions, so dQ is not bit-for-bit
+    reproducible.
     """
     _bshd("q", q)
     _bshd("k", k, q, same_s=False)
@@ -206,11 +217,17 @@ def attn_bwd(q, k, v, out, dout, lse, key_mask=None, scale=None, dq=None, dk=Non
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(k) if dv is None else dv
-    nbytes = attn_bwd_workspace_bytes(B, Sq, H, D)
+    if fused and Sq != Sk:
+        raise ValueError("the fused backward takes equal query and key lengths")
+    nbytes = attn_bwd_fused_workspace_bytes(B, Sq, H, D) if fused else attn_bwd_workspace_bytes(B, Sq, H, D)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     wsb = workspace.numel() * workspace.element_size()
-    if Sq == Sk:
+    if fused:
+        _check(lib().uaa_attn_bwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), B, Sq, H, D, float(scale), _ptr(workspace), wsb,
+                                        _P(_stream(q.device))))
+    elif Sq == Sk:
         _check(lib().uaa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(mask),
                                   _ptr(dq), _ptr(dk), _ptr(dv), B, Sq, H, D, float(scale), _ptr(workspace), wsb,
                                   _P(_stream(q.device))))

@@ -47,82 +47,18 @@
 
 #include <mutex>
 
-#include "uaa_common.cuh"
+#include "attn_bwd_shared.cuh"
 
 namespace uaa {
 
 int validate_attn_sizes(const char* fn, int B, int Sq, int Sk, int H, int D, float scale);
 int check_dev_ptr(const char* fn, const char* name, const void* p);
+int launch_bwd_fused(const void* q, const void* k, const void* v, const void* dout, const uint8_t* mask, int mrows,
+                     void* dq, void* dk, void* dv, int B, int Sq, int Sk, int H, int D, float scale,
+                     const float* delta, const float* nl2, float* dq_acc, cudaStream_t s, const DevCtx& ctx,
+                     int (*mark)(int, cudaStream_t));
 
 namespace {
-
-constexpr int kBT = 128;  // rows per query tile and per key tile
-constexpr int kChunkBytes = 128 * 128;
-constexpr int kComputeThreads = 256;  // warps 0-7
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;    // first MMA issuer (dK/dV kernel: dV / S^T chain; dQ kernel: S chain)
-constexpr int kMmaWarp1 = 10;  // second MMA issuer (dK/dV kernel: dK / dP^T chain; dQ kernel: dQ / dP chain)
-constexpr int kThreads = 352;
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-
-// Warp-collective: the attended-key bits of key tile j of sequence kd (bit c of
-// word t = key c' = 32t + c of the tile); keys past the tile's segment count as
-// masked.  Every lane gets all 4 words.  key_mask is (B, kd.total) in sequence order.
-__device__ __forceinline__ void key_tile_bits(const uint8_t* __restrict__ key_mask, const SeqDesc& kd, int b, int j,
-                                              uint32_t (&w)[4]) {
-  const int lane = threadIdx.x & 31;
-  const SeqTile kt = seq_tile(kd, j);
-  const size_t base = (size_t)b * kd.total + kd.off[kt.seg] + kt.row0;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int c = 32 * t + lane;
-    const bool valid = c < kt.valid && (key_mask == nullptr || key_mask[base + c] != 0);
-    w[t] = __ballot_sync(0xffffffffu, valid);
-  }
-}
-
-__device__ __forceinline__ bool key_tile_any(const uint8_t* __restrict__ key_mask, const SeqDesc& kd, int b, int j) {
-  uint32_t w[4];
-  key_tile_bits(key_mask, kd, b, j, w);
-  return (w[0] | w[1] | w[2] | w[3]) != 0;
-}
-
-// Packed bf16 pairs of 64 consecutive columns -> 32 TMEM columns (two stores).
-__device__ __forceinline__ void store_packed64(uint32_t taddr, const float (&x)[64]) {
-  uint32_t pk[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(x[2 * c], x[2 * c + 1]);
-  tmem_st32_bits(taddr, pk);
-}
-
-struct Item3 {
-  int t, h, b;
-};
-__device__ __forceinline__ Item3 decode_item(int item, int ntiles, int H) {
-  Item3 it;
-  it.t = item % ntiles;
-  const int bh = item / ntiles;
-  it.h = bh % H;
-  it.b = bh / H;
-  return it;
-}
-
-// TMEM column of the A operand for K step kk (16 elements = 8 packed columns)
-// when the 128 packed K elements sit as two runs of 32 columns at base and
-// base + 64 (column half hf of the compute warps writes its 64 elements into
-// the first 32 columns of its own 64-column region).
-__device__ __forceinline__ uint32_t packed_a_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 // ---------------------------------------------------------------------------
 // 1. Delta = rowsum(dO * O) and -LSE*log2e per query row.  Eight lanes per
@@ -196,7 +132,6 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
   }
 }
 
-__host__ __device__ constexpr int padded_rows(int S) { return (S + 127) / 128 * 128; }
 
 // ---------------------------------------------------------------------------
 // 2. dK / dV (K/V-tile-major)
@@ -946,10 +881,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (kMask) {
             const uint32_t w0 = words[2 * hf], w1 = words[2 * hf + 1];
+            if ((w0 & w1) != 0xffffffffu) {  // only tiles with masked (or missing) keys need it
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              if (!((w0 >> c) & 1u)) p[c] = 0.f;
-              if (!((w1 >> c) & 1u)) p[32 + c] = 0.f;
+              for (int c = 0; c < 32; ++c) {
+                if (!((w0 >> c) & 1u)) p[c] = 0.f;
+                if (!((w1 >> c) & 1u)) p[32 + c] = 0.f;
+              }
             }
           } else {
             // the last tile of a key segment is partial: its rows past the segment read as zeros
@@ -1060,7 +997,8 @@ int record_prof(int i, cudaStream_t stream) {
 template <int D, bool kMask>
 int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
                const uint8_t* mask, int mrows, void* dq, void* dk, void* dv, int B, const SeqDesc& qd,
-               const SeqDesc& kd, int H, float scale, float* delta, cudaStream_t stream, const DevCtx& ctx) {
+               const SeqDesc& kd, int H, float scale, float* delta, bool fused, cudaStream_t stream,
+               const DevCtx& ctx) {
   const size_t rows = (size_t)B * qd.total * H;
   const int nqt = qd.tile0[qd.nseg], nkt = kd.tile0[kd.nseg];
   float* nl2 = delta + (size_t)B * H * nqt * kBT;
@@ -1068,6 +1006,12 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
       static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, nl2, qd, B, H);
   int st = check_launch("uaa_attn_bwd (preprocess)");
   if (st) return st;
+  if (fused) {
+    // one K/V-major pass (dQ by reductions into the fp32 accumulator after the two row vectors)
+    float* dq_acc = nl2 + (size_t)B * H * nqt * kBT;
+    return launch_bwd_fused(q, k, v, dout, mask, mrows, dq, dk, dv, B, qd.total, kd.total, H, D, scale, delta, nl2,
+                            dq_acc, stream, ctx, record_prof);
+  }
   SegMaps mq, mk, mv, mdo;
   if ((st = encode_seq_maps(&mq, q, qd, B, H, D, 128))) return st;
   if ((st = encode_seq_maps(&mk, k, kd, B, H, D, 128))) return st;
@@ -1109,9 +1053,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
 // mrows: rows of key_mask; batch b uses row b % mrows
 int bwd_dispatch(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
                  const uint8_t* key_mask, int mrows, void* dq, void* dk, void* dv, int B, const SeqDesc& qd,
-                 const SeqDesc& kd, int H, int D, float scale, float* delta, cudaStream_t s, const DevCtx& ctx) {
-#define UAA_BWD(DD, MM) \
-  launch_bwd<DD, MM>(q, k, v, out, dout, lse, key_mask, mrows, dq, dk, dv, B, qd, kd, H, scale, delta, s, ctx)
+                 const SeqDesc& kd, int H, int D, float scale, float* delta, cudaStream_t s, const DevCtx& ctx,
+                 bool fused = false) {
+#define UAA_BWD(DD, MM)                                                                                        \
+  launch_bwd<DD, MM>(q, k, v, out, dout, lse, key_mask, mrows, dq, dk, dv, B, qd, kd, H, scale, delta, fused, s, \
+                     ctx)
   if (D == 64) return key_mask ? UAA_BWD(64, true) : UAA_BWD(64, false);
   return key_mask ? UAA_BWD(128, true) : UAA_BWD(128, false);
 #undef UAA_BWD
@@ -1209,6 +1155,38 @@ extern "C" int uaa_attn_bwd(const void* q, const void* k, const void* v, const v
                             uaa_stream_t stream) {
   return uaa_attn_bwd_cross(q, k, v, out, dout, lse, key_mask, dq, dk, dv, B, S, S, H, D, scale, workspace,
                             workspace_bytes, stream);
+}
+
+extern "C" size_t uaa_attn_bwd_fused_workspace_bytes(int B, int S, int H, int D) {
+  if (B < 0 || S < 0 || H < 0 || (D != 64 && D != 128)) return 0;
+  // Delta and -LSE*log2e (B, H, S_pad) fp32, then the fp32 dQ accumulator (B, H, S_pad, D)
+  const size_t rows = (size_t)B * H * padded_rows(S);
+  return ((rows * 8 + rows * D * 4) + 255) & ~(size_t)255;
+}
+
+extern "C" int uaa_attn_bwd_fused(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                  const float* lse, const uint8_t* key_mask, void* dq, void* dk, void* dv, int B,
+                                  int S, int H, int D, float scale, void* workspace, size_t workspace_bytes,
+                                  uaa_stream_t stream) {
+  const char* fn = "uaa_attn_bwd_fused";
+  int st = validate_attn_sizes(fn, B, S, S, H, D, scale);
+  if (st) return st;
+  if ((uint64_t)B * H * S == 0) return UAA_OK;
+  if ((st = check_dev_ptr(fn, "q", q)) || (st = check_dev_ptr(fn, "k", k)) || (st = check_dev_ptr(fn, "v", v)) ||
+      (st = check_dev_ptr(fn, "out", out)) || (st = check_dev_ptr(fn, "dout", dout)) ||
+      (st = check_dev_ptr(fn, "dq", dq)) || (st = check_dev_ptr(fn, "dk", dk)) || (st = check_dev_ptr(fn, "dv", dv)))
+    return st;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: lse is NULL or not 4-byte aligned", fn);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return set_error(UAA_ERR_INVALID_ARG, "%s: workspace is NULL or not 256-byte aligned", fn);
+  const size_t need = uaa_attn_bwd_fused_workspace_bytes(B, S, H, D);
+  if (workspace_bytes < need)
+    return set_error(UAA_ERR_INVALID_ARG, "%s: workspace has %zu bytes, %zu needed", fn, workspace_bytes, need);
+  DevCtx ctx;
+  if ((st = get_dev_ctx(&ctx))) return st;
+  return bwd_dispatch(q, k, v, out, dout, lse, key_mask, B, dq, dk, dv, B, seq_plain(S), seq_plain(S), H, D, scale,
+                      static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), ctx, true);
 }
 
 extern "C" int uaa_attn_bwd_groups(const void* q, const void* k, const void* v, const void* out, const void* dout,

@@ -445,9 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t mw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) mw[q] = ctl->mask_words[nv % R][q];
+          // a tile whose keys are all attended (most tiles of a key-padding mask) needs no bias
+          if ((mw[0] & mw[1] & mw[2] & mw[3]) != 0xffffffffu) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+            for (int c = 0; c < kBN; ++c)
+              if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+          }
         } else {
           // the last tile of a segment is partial: its rows past the segment read as zeros
           const int lim = kSeg ? seq_tile_at(kd, j, kseg).valid : ((j + 1) * kBN > Sk ? Sk - j * kBN : kBN);

@@ -9,9 +9,9 @@
 // Summary / Performance: the exchange around the attention module is the part
 // whose speed matters (7518 us -> 6762 us per layer on 4 H800s).
 //
-// These kernels are HBM-bound copies: 16-byte vector loads and stores, each
-// thread moving kUnroll vectors per loop trip with all loads issued before the
-// stores, and a grid of a multiple of the SM count.  Algorithmic bytes = one
+// These kernels are HBM-bound copies: one warp per output row, 16-byte vector
+// loads and stores, each lane moving kUnroll vectors per loop trip with all
+// loads issued before the stores, and a grid of a multiple of the SM count.  Algorithmic bytes = one
 // read + one write of every valid element (+ one write of every padding
 // element in the inverse).
 #include "uaa_common.cuh"
@@ -36,82 +36,79 @@ __device__ __forceinline__ int find_shard(const Partition& part, int n) {
   return p;
 }
 
-// y[g, b, n, h', :] = x[p, b, s, g*Hg + h', :] with n = offs[p] + s, and 0 for
-// the padding heads g*Hg + h' >= H (Hg = ceil(H/P)).
-// Index space = output vectors, in output order (g, b, n, h', v).
-__global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const uint4* __restrict__ x, uint4* __restrict__ y,
-                                                               const __grid_constant__ Partition part, int B,
-                                                               int H, int Hg, int rowvec, uint32_t total) {
-  const int N = part.offs[part.P];
-  const uint32_t run = (uint32_t)Hg * rowvec;  // contiguous vectors of one (g, b, n) row
-  const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < total; base += stride * kUnroll) {
+// One warp copies a run of n 16-byte vectors (or writes n zero vectors when src is
+// null), each lane moving up to kUnroll vectors per trip with all loads issued first.
+__device__ __forceinline__ void copy_run(const uint4* __restrict__ src, uint4* __restrict__ dst, int n, int lane) {
+  for (int v0 = lane; v0 < n; v0 += 32 * kUnroll) {
     uint4 v[kUnroll];
-    uint32_t dst[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t idx = base + (uint32_t)u * stride;
-      dst[u] = idx;
-      if (idx < total) {
-        const uint32_t w = idx % run;
-        uint32_t r = idx / run;
-        const int n = (int)(r % (uint32_t)N);
-        r /= (uint32_t)N;
-        const int b = (int)(r % (uint32_t)B);
-        const int g = (int)(r / (uint32_t)B);
-        const int p = find_shard(part, n);
-        const int s = n - part.offs[p];
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if ((uint32_t)g * run + w < (uint32_t)H * rowvec) {  // a real head, not padding
-          const size_t src = (((size_t)p * B + b) * part.cap + s) * (size_t)H * rowvec + (size_t)g * run + w;
-          v[u] = __ldcs(x + src);
-        }
-      }
+      const int i = v0 + 32 * u;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (src && i < n) v[u] = __ldcs(src + i);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (dst[u] < total) __stcs(y + dst[u], v[u]);
+      if (v0 + 32 * u < n) __stcs(dst + v0 + 32 * u, v[u]);
+  }
+}
+
+// y[g, b, n, h', :] = x[p, b, s, g*Hg + h', :] with n = offs[p] + s, and 0 for
+// the padding heads g*Hg + h' >= H (Hg = ceil(H/P)).
+// One warp per output row (g, b, n): the row's Hg*rowvec vectors are one
+// contiguous run of the source row as well, so the index arithmetic (two
+// divisions and the shard search) is paid once per row, not per vector.
+__global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const uint4* __restrict__ x, uint4* __restrict__ y,
+                                                               const __grid_constant__ Partition part, int B,
+                                                               int H, int Hg, int rowvec, uint32_t rows) {
+  const int N = part.offs[part.P];
+  const int run = Hg * rowvec;
+  const int lane = threadIdx.x & 31;
+  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const int n = (int)(r % (uint32_t)N);
+    const uint32_t gb = r / (uint32_t)N;
+    const int b = (int)(gb % (uint32_t)B);
+    const int g = (int)(gb / (uint32_t)B);
+    const int p = find_shard(part, n);
+    const int s = n - part.offs[p];
+    const int heads = H - g * Hg < Hg ? H - g * Hg : Hg;  // real heads of this group (may be <= 0)
+    const int real = heads > 0 ? heads * rowvec : 0;
+    uint4* dst = y + (size_t)r * run;
+    const uint4* src = x + (((size_t)p * B + b) * part.cap + s) * (size_t)H * rowvec + (size_t)g * run;
+    copy_run(src, dst, real, lane);
+    copy_run(nullptr, dst + real, run - real, lane);
   }
 }
 
 // x[p, b, s, h, :] = y[h / Hg, b, offs[p] + s, h % Hg, :] for s < L_p, else 0
 // (h < H only: the padding heads of the groups are dropped).
-// Index space = output vectors, in output order (p, b, s, h, v), padding rows included.
+// One warp per output row (p, b, s): the row is P contiguous runs, one per head
+// group, each a contiguous run of that group's row n = offs[p] + s.
 __global__ void __launch_bounds__(kThreads) head_to_seq_kernel(const uint4* __restrict__ y, uint4* __restrict__ x,
                                                                const __grid_constant__ Partition part, int B,
-                                                               int H, int Hg, int rowvec, uint32_t total) {
+                                                               int H, int Hg, int rowvec, uint32_t rows) {
   const int N = part.offs[part.P];
-  const uint32_t rowlen = (uint32_t)H * rowvec;
-  const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < total; base += stride * kUnroll) {
-    uint4 v[kUnroll];
-    uint32_t dst[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t idx = base + (uint32_t)u * stride;
-      dst[u] = idx;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (idx < total) {
-        const uint32_t w = idx % rowlen;
-        uint32_t r = idx / rowlen;
-        const int s = (int)(r % (uint32_t)part.cap);
-        r /= (uint32_t)part.cap;
-        const int b = (int)(r % (uint32_t)B);
-        const int p = (int)(r / (uint32_t)B);
-        if (s < part.offs[p + 1] - part.offs[p]) {
-          const int h = (int)(w / (uint32_t)rowvec);
-          const int vv = (int)(w % (uint32_t)rowvec);
-          const int g = h / Hg;
-          const int hh = h - g * Hg;
-          const size_t src =
-              ((((size_t)g * B + b) * N + part.offs[p] + s) * Hg + hh) * (size_t)rowvec + vv;
-          v[u] = __ldcs(y + src);
-        }
-      }
+  const int rowlen = H * rowvec;
+  const int lane = threadIdx.x & 31;
+  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const int s = (int)(r % (uint32_t)part.cap);
+    const uint32_t pb = r / (uint32_t)part.cap;
+    const int b = (int)(pb % (uint32_t)B);
+    const int p = (int)(pb / (uint32_t)B);
+    uint4* dst = x + (size_t)r * rowlen;
+    if (s >= part.offs[p + 1] - part.offs[p]) {  // transport padding
+      copy_run(nullptr, dst, rowlen, lane);
+      continue;
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (dst[u] < total) __stcs(x + dst[u], v[u]);
+    const int n = part.offs[p] + s;
+#pragma unroll 1
+    for (int g = 0; g * Hg < H; ++g) {
+      const int heads = H - g * Hg < Hg ? H - g * Hg : Hg;
+      const uint4* src = y + (((size_t)g * B + b) * N + n) * (size_t)Hg * rowvec;
+      copy_run(src, dst + (size_t)g * Hg * rowvec, heads * rowvec, lane);
+    }
   }
 }
 
@@ -133,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) assemble_key_mask_kernel(const uint8
 
 // x[z, s, :] = 0 for the padding rows len[p] <= s < cap of every slab z = p*B + b of a
 // (nseg*B, cap, H, D) bf16 buffer; one thread per 16-byte vector.
-__global__ void __launch_bounds__(kThreads) zero_pad_kernel(uint4* __restrict__ x, const SeqDesc d, int B,
+__global__ void __launch_bounds__(kThreads) zero_pad_kernel(uint4* __restrict__ x, const __grid_constant__ SeqDesc d, int B,
                                                             int rowvec, int maxpad, uint64_t total) {
   const uint64_t per_slab = (uint64_t)maxpad * rowvec;
   for (uint64_t idx = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -147,16 +144,12 @@ __global__ void __launch_bounds__(kThreads) zero_pad_kernel(uint4* __restrict__ 
 }
 
 int sm_count() {
-  static int cached = 0;
-  if (!cached) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) ==
-                                                  cudaSuccess && n > 0)
-      cached = n;
-    else
-      return 148;
-  }
-  return cached;
+  // per device: the attribute query is cheap, and a process may drive GPUs of different sizes
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess || n <= 0)
+    return 148;
+  return n;
 }
 
 int grid_for(uint64_t work_items, int items_per_thread) {
@@ -236,10 +229,10 @@ int uaa_seq_to_head(const void* x, void* y, int P, const int* shard_lens, int ca
   int rowvec = 0, Hg = 0;
   int st = relayout_common("uaa_seq_to_head", x, y, P, shard_lens, cap, B, H, D, elem_bytes, &part, &rowvec, &Hg);
   if (st) return st;
-  const uint32_t total = (uint32_t)((uint64_t)P * B * part.offs[P] * Hg * rowvec);
-  if (total == 0) return UAA_OK;
-  seq_to_head_kernel<<<grid_for(total, kUnroll), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(x), static_cast<uint4*>(y), part, B, H, Hg, rowvec, total);
+  const uint32_t rows = (uint32_t)((uint64_t)P * B * part.offs[P]);
+  if (rows == 0) return UAA_OK;
+  seq_to_head_kernel<<<grid_for((uint64_t)rows * 32, 1), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(x), static_cast<uint4*>(y), part, B, H, Hg, rowvec, rows);
   return check_launch("uaa_seq_to_head");
 }
 
@@ -249,10 +242,10 @@ int uaa_head_to_seq(const void* y, void* x, int P, const int* shard_lens, int ca
   int rowvec = 0, Hg = 0;
   int st = relayout_common("uaa_head_to_seq", y, x, P, shard_lens, cap, B, H, D, elem_bytes, &part, &rowvec, &Hg);
   if (st) return st;
-  const uint32_t total = (uint32_t)((uint64_t)P * B * cap * H * rowvec);
-  if (total == 0) return UAA_OK;
-  head_to_seq_kernel<<<grid_for(total, kUnroll), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(y), static_cast<uint4*>(x), part, B, H, Hg, rowvec, total);
+  const uint32_t rows = (uint32_t)((uint64_t)P * B * cap);
+  if (rows == 0 || H == 0) return UAA_OK;
+  head_to_seq_kernel<<<grid_for((uint64_t)rows * 32, 1), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(y), static_cast<uint4*>(x), part, B, H, Hg, rowvec, rows);
   return check_launch("uaa_head_to_seq");
 }
 
