@@ -42,11 +42,12 @@ from ulysses_dit_attention_gb300 import synth  # noqa: E402
 
 WORKLOAD = "ulysses_p4_n27280_h40_d128"
 
-# DRAM bytes (read + write) per attn_bwd_dkdv_kernel launch (all four 10-head groups of the workload
-# above): the ncu capture of the same launch at 2 heads per group (profiles/), scaled by the five
-# times as many work items; keyed by the SHA-256 prefix of the attn_bwd.cu it was taken on, so the
-# bench reports null once the kernel source has changed since.
-DKDV_TRAFFIC = {"3e6839845bb7ccbc": 5 * (226782208 + 83292160)}
+# DRAM bytes (read + write) per attn_bwd_dkdv_kernel launch of the workload above (all four
+# 10-head groups in one launch), from a one-pass ncu capture of the full-size launch
+# (dram__bytes_read.sum 1.13 GB + dram__bytes_write.sum 533.93 MB, as printed to three digits);
+# keyed by the SHA-256 prefix of the attn_bwd.cu it was taken on, so the bench reports null once
+# the kernel source has changed since.
+DKDV_TRAFFIC = {"173aee873844b213": 1130000000 + 533930000}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
