@@ -139,3 +139,29 @@ def test_fused_ulysses_rejects_bad_partitions_on_host(L):
     tiles = 2 + 1 + 1
     assert L.uaa_ulysses_attn_bwd_workspace_bytes(3, ok, 130, 2, 5, 64) == (2 * 5 * tiles * 128 * 8 + 255) // 256 * 256
     assert L.uaa_ulysses_attn_bwd_workspace_bytes(9, lens9, 10, 1, 2, 128) == 0
+
+
+def test_grouped_and_one_pass_backward_validate_on_host(L):
+    fake = ctypes.c_void_p(1 << 20)
+    f = ctypes.c_float(0.125)
+    # the grouped calls need G >= 1 and G*B <= 65535
+    assert L.uaa_attn_fwd_groups(fake, fake, fake, None, fake, fake, 0, 2, 128, 2, 64, f, None) == -1
+    assert "G=0" in _err()
+    assert L.uaa_attn_fwd_groups(fake, fake, fake, None, fake, fake, 300, 300, 128, 2, 64, f, None) == -2
+    assert L.uaa_attn_bwd_groups(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, 4, 2, 128, 2, 64, f,
+                                 fake, 16, None) == -1
+    assert "workspace" in _err()
+    # grouped backward workspace: the plain backward's for a batch of G*B
+    assert L.uaa_attn_bwd_workspace_bytes(8, 300, 2, 64) == (8 * 2 * 384 * 8 + 255) // 256 * 256
+    # one-pass backward: the two row vectors plus an fp32 (B, H, S_pad, D) dQ accumulator
+    B, S, H, D = 2, 300, 3, 128
+    rows = B * H * 384
+    assert L.uaa_attn_bwd_fused_workspace_bytes(B, S, H, D) == (rows * 8 + rows * D * 4 + 255) // 256 * 256
+    assert L.uaa_attn_bwd_fused_workspace_bytes(B, S, H, 96) == 0
+    need = L.uaa_attn_bwd_fused_workspace_bytes(B, S, H, D)
+    assert L.uaa_attn_bwd_fused(fake, fake, fake, fake, fake, fake, None, fake, fake, fake, B, S, H, D, f, fake,
+                                need - 256, None) == -1
+    assert "workspace" in _err()
+    # the diagnostic load-drop knob takes any value and is switched off by a negative one
+    L.uaa_debug_drop_load(3)
+    L.uaa_debug_drop_load(-1)
