@@ -711,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&ctl->bar_kv_empty[nk % R]);
       mma_commit(&ctl->bar_kv_empty[(nk + 1) % R]);
     };
-    // dP_gg = dO V^T (A = dO in TMEM); V_gg is read only by this GEMM
+    // dP_gg = dO V^T (A = dO in TMEM); V_gg is read only by this GEMM.  dP is on the
+    // critical path (dP -> dS -> dQ -> next dP), so the turn passes only after its
+    // last MMA: S MMAs issued earlier would be interleaved with it and delay it.
     auto issue_dp = [&](uint32_t gg, bool pass) {
       const uint32_t nv = 2 * gg + 1;
       const uint64_t b0 = sdesc_sw128(ring(nv), 16, 1024);
@@ -719,8 +721,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
         mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
-        if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
       }
+      if (pass) pass_turn();
       mma_commit(&ctl->bar_dp_full);
       mma_commit(&ctl->bar_kv_empty[nv % R]);
     };
