@@ -552,9 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 3. dQ (Q-tile-major)
 template <int D>
 struct DqLayout {
-  static constexpr int kRing = (D == 128) ? 6 : 8;
+  // K and V tiles in rings of their own: a K slot is freed only by dQ (late in a key
+  // tile's processing), a V slot already by dP, so V gets fewer slots and K more
+  static constexpr int kKRing = (D == 128) ? 4 : 7;
+  static constexpr int kVRing = (D == 128) ? 3 : 6;
+  static constexpr int kRing = kKRing + kVRing;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kRingOff = 0;  // K_j, V_j, K_j+1, ... (Q and dO live in TMEM)
+  static constexpr int kRingOff = 0;  // K slots, then V slots (Q and dO live in TMEM)
   static constexpr int kCtl = kRingOff + kRing * kTileBytes;
   static constexpr int kSmem = kCtl + 512;
   static_assert(kSmem <= 232448, "dQ shared memory exceeds the per-CTA limit");
@@ -562,7 +566,7 @@ struct DqLayout {
 
 struct DqCtl {
   uint64_t bar_qdo_ready;
-  uint64_t bar_kv_full[8], bar_kv_empty[8];
+  uint64_t bar_kv_full[16], bar_kv_empty[16];
   uint64_t bar_s_full, bar_s_read, bar_dp_full, bar_ds_ready;
   uint64_t bar_dq_done, bar_dq_free, bar_final[2];
   uint32_t tmem_base;
@@ -583,6 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = DqLayout<D>;
   constexpr int kChunks = D / 64;
   constexpr int R = L::kRing;
+  constexpr int KR = L::kKRing, VR = L::kVRing;
+  // slot and use of key tile g's K and V
+  auto kslot = [](uint32_t g) { return (int)(g % KR); };
+  auto vslot = [](uint32_t g) { return KR + (int)(g % VR); };
+  auto kpar = [](uint32_t g) { return (g / KR) & 1u; };
+  auto vpar = [](uint32_t g) { return (g / VR) & 1u; };
   constexpr uint32_t kIdescKK = idesc_bf16_f32(128, kBT, false, false);  // S, dP
   constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dQ (A in TMEM)
   // TMEM: S, dP (then dS), the dQ accumulator, and Q / dO as A operands of S / dP
@@ -605,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->bar_qdo_ready, kComputeThreads);
     for (int s = 0; s < R; ++s) {
       mbar_init(&ctl->bar_kv_full[s], 1);
-      mbar_init(&ctl->bar_kv_empty[s], 2);  // one release per issuer
+      mbar_init(&ctl->bar_kv_empty[s], s < KR ? 2 : 1);  // K: S and dQ read it; V: dP only
     }
     mbar_init(&ctl->bar_s_full, 1);
     // the compute warps plus the other issuer's hand-over (see the issuers)
@@ -634,13 +644,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  uint32_t kv_armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint32_t kv_armed[16] = {};
   bool mma_issued = false;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    uint32_t n = 0, it = 0;
+    uint32_t n = 0, it = 0, gp = 0;  // n: loads, gp: key tiles loaded
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
       SeqCursor kseg;  // key segment cursor (tiles are visited in order)
@@ -652,8 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
-          const int slot = n % R;
-          const uint32_t use = n / R;
+          const int slot = kind == 0 ? kslot(gp) : vslot(gp);
+          const uint32_t use = kind == 0 ? gp / KR : gp / VR;
           if (lane == 0 && use > 0) ok = wait_or_abort(&ctl->bar_kv_empty[slot], (use - 1) & 1, ctx, ctl);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -673,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             kv_armed[slot] = use + 1;
           }
         }
+        ++gp;
       }
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp1) {
@@ -694,13 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = warp - kMmaWarp;  // 0: chain s, 1: chain d
     bool ok = true;
     uint32_t g = 0, it = 0;  // g: processed key tiles across items
-    auto ring = [&](uint32_t n) { return sbase + L::kRingOff + (n % R) * L::kTileBytes; };
+    auto slot_addr = [&](int slot) { return sbase + L::kRingOff + slot * L::kTileBytes; };
     // hand the turn to the other chain (see above)
     auto pass_turn = [&]() { mbar_arrive(c == 0 ? &ctl->bar_ds_ready : &ctl->bar_s_read); };
     // S_gg = Q K^T (A = Q in TMEM); releases (this thread's share of) the slots of K_gg and V_gg
     auto issue_s = [&](uint32_t gg, bool pass) {
-      const uint32_t nk = 2 * gg;
-      const uint64_t b0 = sdesc_sw128(ring(nk), 16, 1024);
+      const uint64_t b0 = sdesc_sw128(slot_addr(kslot(gg)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
@@ -708,15 +718,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
       }
       mma_commit(&ctl->bar_s_full);
-      mma_commit(&ctl->bar_kv_empty[nk % R]);
-      mma_commit(&ctl->bar_kv_empty[(nk + 1) % R]);
+      mma_commit(&ctl->bar_kv_empty[kslot(gg)]);
     };
     // dP_gg = dO V^T (A = dO in TMEM); V_gg is read only by this GEMM.  dP is on the
     // critical path (dP -> dS -> dQ -> next dP), so the turn passes only after its
     // last MMA: S MMAs issued earlier would be interleaved with it and delay it.
     auto issue_dp = [&](uint32_t gg, bool pass) {
-      const uint32_t nv = 2 * gg + 1;
-      const uint64_t b0 = sdesc_sw128(ring(nv), 16, 1024);
+      const uint64_t b0 = sdesc_sw128(slot_addr(vslot(gg)), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
@@ -724,19 +732,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (pass) pass_turn();
       mma_commit(&ctl->bar_dp_full);
-      mma_commit(&ctl->bar_kv_empty[nv % R]);
+      mma_commit(&ctl->bar_kv_empty[vslot(gg)]);
     };
     // dQ += dS K_gg (A = dS in the dP columns)
     auto issue_dq = [&](uint32_t gg, bool first, bool pass) {
-      const uint32_t nk = 2 * gg;
-      const uint64_t b0 = sdesc_sw128(ring(nk), kChunkBytes, 1024);
+      const uint64_t b0 = sdesc_sw128(slot_addr(kslot(gg)), kChunkBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kBT / 16; ++kk) {
         mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
                     (!first || kk > 0) ? 1u : 0u);
         if (pass && kk == kBT / 16 - 5) pass_turn();
       }
-      mma_commit(&ctl->bar_kv_empty[nk % R]);
+      mma_commit(&ctl->bar_kv_empty[kslot(gg)]);
     };
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
@@ -759,8 +766,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // have seen K / V of the next tile land, so no other wait is needed.
         ok = wait_or_abort(&ctl->bar_qdo_ready, it & 1, ctx, ctl);
         if (ok) {
-          const uint32_t n0 = 2 * g + (uint32_t)c;  // K_g for chain s, V_g for chain d
-          ok = wait_or_abort(&ctl->bar_kv_full[n0 % R], (n0 / R) & 1, ctx, ctl);
+          // K_g for chain s, V_g for chain d
+          ok = c == 0 ? wait_or_abort(&ctl->bar_kv_full[kslot(g)], kpar(g), ctx, ctl)
+                      : wait_or_abort(&ctl->bar_kv_full[vslot(g)], vpar(g), ctx, ctl);
         }
         if (ok) {
           tc_fence_after();
@@ -859,9 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           has_next = jn < nkt;
         }
         if (has_next) {
-          const uint32_t nk1 = 2 * (g + 1), nv1 = nk1 + 1;
-          bool okw = wait_or_abort(&ctl->bar_kv_full[nk1 % R], (nk1 / R) & 1, ctx, ctl);
-          if (okw) okw = wait_or_abort(&ctl->bar_kv_full[nv1 % R], (nv1 / R) & 1, ctx, ctl);
+          bool okw = wait_or_abort(&ctl->bar_kv_full[kslot(g + 1)], kpar(g + 1), ctx, ctl);
+          if (okw) okw = wait_or_abort(&ctl->bar_kv_full[vslot(g + 1)], vpar(g + 1), ctx, ctl);
           ok = __all_sync(0xffffffffu, okw);
           if (!ok) break;
         }
