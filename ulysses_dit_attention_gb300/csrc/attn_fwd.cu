@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Teardown bookkeeping of the producer: uses armed per barrier.
   uint32_t kv_armed[5] = {0, 0, 0, 0, 0};
   uint32_t q_armed = 0;
-  bool mma_issued = false;
+  bool mma_issued = false;  // set in the issuing lane once it has issued an MMA
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -296,11 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the schedule (named barriers take whole warps); lane 0
-    // issues.  Within an item this warp executes no memory instruction: it learns
-    // that P_t is in TMEM from named barrier kBarP + t, which the softmax
-    // warpgroup of tile t arrives on.
-    const bool leader = lane == 0;
+    // The whole warp runs the schedule (named barriers take whole warps) and
+    // computes every UMMA descriptor; one elected lane waits and issues.  Keeping
+    // the descriptor arithmetic warp-uniform, outside any lane-divergent branch,
+    // keeps each issue short: written as a one-lane branch, an MMA issue took
+    // ~80 cycles beside busy softmax warps, more than the 64 the MMA runs.
+    // Within an item this warp executes no memory instruction: it learns that
+    // P_t is in TMEM from named barrier kBarP + t, which the softmax warpgroup of
+    // tile t arrives on.
+    uint32_t el_lane;
+    const bool el = elect_one_sync(&el_lane);
     bool ok = true;
     uint32_t g = 0;   // global tile counter across items (phase index of s/pv barriers)
     uint32_t ne = 0;  // items with at least one attended key tile (phases of q_full, o_free)
@@ -313,9 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-        mma_bf16(d, desc_add(dq0, off), desc_add(dk0, off), kIdescS, kk > 0);
+        const uint64_t a = desc_add(dq0, off), b = desc_add(dk0, off);
+        if (el) mma_bf16(d, a, b, kIdescS, kk > 0);
       }
-      mma_commit(&ctl->bar_s_full[t]);
+      if (el) mma_commit(&ctl->bar_s_full[t]);
     };
     auto issue_pv = [&](int t, uint32_t nv, bool acc) {
       const uint32_t aP = tmem + (uint32_t)(t * kBN);  // P_t: 128 rows x 128 keys bf16 = 64 columns
@@ -323,9 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d = tmem + 256 + (uint32_t)(t * D);
       const uint64_t dv0 = sdesc_sw128(sV, kChunkBytes, 1024);
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_bf16_ts(d, aP + kk * 8, desc_add(dv0, kk * 2048), kIdescPV, (acc || kk > 0) ? 1u : 0u);
-      mma_commit(&ctl->bar_pv_done[t]);
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint64_t b = desc_add(dv0, kk * 2048);
+        if (el) mma_bf16_ts(d, aP + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      }
+      if (el) mma_commit(&ctl->bar_pv_done[t]);
     };
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
       // an item without an attended key tile takes no MMA and no barrier
@@ -337,18 +345,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t nk = 2 * g;  // K_0 of this item
       if (ok) {
         bool w = true;
-        if (leader) {
+        if (el) {
           w = wait_or_abort(&ctl->bar_q_full, ne & 1, ctx, ctl);
           if (w) w = wait_or_abort(&ctl->bar_kv_full[nk % R], (nk / R) & 1, ctx, ctl);
-          if (w) {
-            tc_fence_after();
-            issue_s(0, nk);
-            issue_s(1, nk);
+        }
+        ok = __shfl_sync(0xffffffffu, w, el_lane);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, nk);
+          issue_s(1, nk);
+          if (el) {
             mma_commit(&ctl->bar_kv_empty[nk % R]);
             mma_issued = true;
           }
         }
-        ok = __shfl_sync(0xffffffffu, w, 0);
       }
       for (int j = 0; j < nt; ++j) {
         const uint32_t gj = g + j;
@@ -361,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && j == 0 && ne > 0) {
           // the previous item's epilogue must have read O before PV0_0 overwrites it
           bool w = true;
-          if (leader) w = wait_or_abort(&ctl->bar_o_free, (ne - 1) & 1, ctx, ctl);
-          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (el) w = wait_or_abort(&ctl->bar_o_free, (ne - 1) & 1, ctx, ctl);
+          ok = __shfl_sync(0xffffffffu, w, el_lane);
         }
-        if (ok && leader) {
+        if (ok) {
           tc_fence_after();
           issue_pv(0, nv, j > 0);
           if (more) issue_s(0, nk1);
@@ -372,19 +382,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // tile 1: PV1_j, then S1_{j+1}
         named_sync(kBarP + 1, kBarPCount);
-        if (ok && leader) {
+        if (ok) {
           tc_fence_after();
           issue_pv(1, nv, j > 0);
-          mma_commit(&ctl->bar_kv_empty[nv % R]);
+          if (el) mma_commit(&ctl->bar_kv_empty[nv % R]);
           if (more) {
             issue_s(1, nk1);
-            mma_commit(&ctl->bar_kv_empty[nk1 % R]);
+            if (el) mma_commit(&ctl->bar_kv_empty[nk1 % R]);
           }
         }
         __syncwarp();
       }
       // both Q tiles are free once this item's MMAs are done
-      if (ok && leader) mma_commit(&ctl->bar_q_empty);
+      if (ok && el) mma_commit(&ctl->bar_q_empty);
       __syncwarp();
       g += nt;
       ++ne;
@@ -551,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stay bounded.
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp && lane == 0 && mma_issued) {
+  if (warp == kMmaWarp && mma_issued) {
     // every MMA has completed before TMEM is released
     mma_commit(&ctl->bar_final);
     settle(&ctl->bar_final, 0, ctx);

@@ -91,6 +91,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// One lane of a converged warp is elected (elect.sync over the full mask): true
+// in that lane only; its lane index is written to *lane.  Tensor-core issuers use
+// it so that the whole warp computes the (uniform) UMMA descriptors and only the
+// issue itself is predicated, rather than running the issue code in a
+// lane-divergent branch.
+__device__ __forceinline__ bool elect_one_sync(uint32_t* lane) {
+  uint32_t l, p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync %0|e, 0xffffffff;\n\t"
+      "selp.u32 %1, 1, 0, e;\n\t}"
+      : "=r"(l), "=r"(p));
+  *lane = l;
+  return p != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
