@@ -53,6 +53,11 @@ constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;
+// One column pair of P in kExpFmaEvery takes its exponentials from exp2_fma2
+// (FMA pipe) instead of ex2 (special-function unit): with two 128-row query
+// tiles per CTA, the 2 x 128 x 128 exponentials of a key-tile step take as
+// many special-function cycles as the step's four GEMMs take tensor cycles.
+constexpr int kExpFmaEvery = 8;
 // named barrier kBarP + t: "P_t is in TMEM" (the 128 threads of softmax warpgroup t
 // arrive, the issuer warp syncs)
 constexpr uint32_t kBarP = 1;
@@ -500,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float2 x = fma2(make_float2(s[64 * hh + 2 * c], s[64 * hh + 2 * c + 1]), c2, nm2);
-            const float2 e = make_float2(ex2(x.x), ex2(x.y));
+            const float2 e =
+                (c % kExpFmaEvery == kExpFmaEvery - 1) ? exp2_fma2(x) : make_float2(ex2(x.x), ex2(x.y));
             rs2 = add2(rs2, e);
             pk[c] = pack_bf16(e.x, e.y);
           }

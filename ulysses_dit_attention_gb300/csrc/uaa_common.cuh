@@ -388,6 +388,28 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
   return *reinterpret_cast<float2*>(&d);
 }
+
+// 2^x for a pair of x <= 8 (x may be -inf), on the FMA pipe instead of the
+// special-function unit.  x is clamped to -127 and split as x = n + f with
+// n = rint(x) (adding 1.5 * 2^23 leaves n in the low mantissa bits) and
+// |f| <= 1/2; 2^f is a cubic fitted in relative error on [-1/2, 1/2]
+// (coefficients from ulysses_dit_attention_gb300/exp2_fit.py, relative error
+// below 8e-5 in float32) and 2^n is built in the exponent field, which gives
+// exactly 0 for n = -127 (so for -inf).
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 9.999280572e-01f, c1 = 6.932610273e-01f, c2 = 2.426113784e-01f, c3 = 5.517164618e-02f;
+  x = make_float2(fmaxf(x.x, -127.f), fmaxf(x.y, -127.f));
+  const float2 t = add2(x, make_float2(kShift, kShift));
+  const float2 f = sub2(x, sub2(t, make_float2(kShift, kShift)));
+  float2 p = fma2(make_float2(c3, c3), f, make_float2(c2, c2));
+  p = fma2(p, f, make_float2(c1, c1));
+  p = fma2(p, f, make_float2(c0, c0));
+  const float2 sc = make_float2(__uint_as_float((__float_as_uint(t.x) << 23) + 0x3f800000u),
+                                __uint_as_float((__float_as_uint(t.y) << 23) + 0x3f800000u));
+  return mul2(p, sc);
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
