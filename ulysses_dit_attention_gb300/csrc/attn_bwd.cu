@@ -32,11 +32,13 @@
 // Keys outside the mask get P = 0, hence dK = dV = 0 exactly; key tiles with
 // no attended key are skipped (the dK/dV kernel writes zeros for them).
 //
-// Warp roles in both main kernels: warps 0-7 compute (TMEM lane quadrant =
-// warp % 4, column half = warp / 4), warp 8 TMA producer, warp 9 tcgen05
-// issuer and warp 10 a second issuer, the two taking turns burst by burst.  An
-// MMA that overwrites TMEM columns an earlier MMA of the same thread reads is
-// issued after it: the MMAs of one thread execute in order.
+// Warp roles: warps 0-7 compute (TMEM lane quadrant = warp % 4, column half =
+// warp / 4), warp 8 TMA producer; the dK/dV kernel's tcgen05 issuer is warp 9
+// (one elected lane), the dQ kernel's are warps 9 and 10 (lane 0 of each).
+// MMAs of one thread execute in order; an MMA that reads its A operand from
+// TMEM is not, however, ordered before a later MMA that overwrites those
+// columns (with the A operand in shared memory it is), so the one such pair
+// (dQ_g, then dP_{g+1} in the dQ kernel) is separated by a completion wait.
 //
 // Query and key sequences are segmented (SeqDesc): a plain (B, S, H, D)
 // tensor is one segment; the sequence shards of a Ulysses step are P segments,
@@ -59,6 +61,10 @@ int launch_bwd_fused(const void* q, const void* k, const void* v, const void* do
                      int (*mark)(int, cudaStream_t));
 
 namespace {
+
+// The dK/dV kernel: warps 0-7 compute, warp 8 TMA producer, warp 9 the tcgen05
+// issuer (the dQ kernel has a second issuer, warp 10: kThreads).
+constexpr int kSplitThreads = 320;
 
 // ---------------------------------------------------------------------------
 // 1. Delta = rowsum(dO * O) and -LSE*log2e per query row.  Eight lanes per
@@ -156,14 +162,14 @@ struct DkdvCtl {
   uint64_t bar_q_full[3], bar_q_empty[3];
   uint64_t bar_do_full[2], bar_do_empty[2];
   uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready;
-  uint64_t bar_acc_done, bar_acc_free, bar_final[2];
+  uint64_t bar_acc_done, bar_acc_free, bar_final;
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(DkdvCtl) <= 256, "control block");
 
 template <int D, bool kMask>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSplitThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ SegMaps tmQ, const __grid_constant__ SegMaps tmK,
                          const __grid_constant__ SegMaps tmV, const __grid_constant__ SegMaps tmDO,
                          const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
@@ -195,9 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint8_t* mask = kMask ? key_mask : nullptr;
 
   if (threadIdx.x == 0) {
-    // buffers read by both issuers (K/V, Q_i, dO_i) are released by a commit of each
+    // a Q_i / dO_i stage is read by two GEMMs, each releasing it by a commit
     mbar_init(&ctl->bar_kv_full, 1);
-    mbar_init(&ctl->bar_kv_empty, 2);
+    mbar_init(&ctl->bar_kv_empty, 1);
     for (int s = 0; s < L::kQStages; ++s) {
       mbar_init(&ctl->bar_q_full[s], 1);
       mbar_init(&ctl->bar_q_empty[s], 2);
@@ -208,13 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->bar_s_full, 1);
     mbar_init(&ctl->bar_dp_full, 1);
-    // the compute warps plus the other issuer's hand-over (see the issuers)
-    mbar_init(&ctl->bar_p_ready, kComputeThreads + 1);
-    mbar_init(&ctl->bar_ds_ready, kComputeThreads + 1);
-    mbar_init(&ctl->bar_acc_done, 2);
+    mbar_init(&ctl->bar_p_ready, kComputeThreads);
+    mbar_init(&ctl->bar_ds_ready, kComputeThreads);
+    mbar_init(&ctl->bar_acc_done, 1);
     mbar_init(&ctl->bar_acc_free, kComputeThreads);
-    mbar_init(&ctl->bar_final[0], 1);
-    mbar_init(&ctl->bar_final[1], 1);
+    mbar_init(&ctl->bar_final, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -297,99 +301,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++it;
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
-    // ------------------------------------------------------------ MMA issuers (lane 0 of warps 9 and 10)
-    // The four GEMMs of a query tile form two chains, each issued by its own
-    // thread:
-    //   warp 9  (chain v): S^T_0 | dV_0 S^T_1 | dV_1 S^T_2 | ...   (after p_ready)
-    //   warp 10 (chain k): dP^T_0 | dK_0 dP^T_1 | dK_1 dP^T_2 | ... (after ds_ready)
-    // The two threads take turns burst by burst, so the tensor pipe runs v, k,
-    // v, k, ... and each thread waits while the other's burst runs.  The turn
-    // is handed over through the handshake barriers themselves: chain k arrives
-    // on p_ready(i) once it has issued all but four MMAs of the burst holding
-    // dP^T_i, chain v on ds_ready(i) once it has done so for the burst holding
-    // dV_i, so each thread's one wait per burst covers both the compute warps'
-    // handshake and its turn.  The tensor pipe queues only about one MMA, and a
-    // single issuing thread that stopped to wait between GEMMs would leave it
-    // idle for a few hundred cycles per wait.  Within a chain the MMAs of one
-    // thread execute in order: dV_i reads P^T_i before S^T_{i+1} overwrites
-    // those columns, and dK_i reads dS^T_i before dP^T_{i+1} does.
-    const int c = warp - kMmaWarp;  // 0: chain v, 1: chain k
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (warp 9)
+    // One elected lane issues the four GEMMs of every query tile i in the order
+    //   S^T_0 dP^T_0 | dV_0 S^T_1 | dK_0 dP^T_1 | dV_1 S^T_2 | dK_1 dP^T_2 | ...
+    // each burst after the compute warps' handshake it depends on: dV_i and
+    // S^T_{i+1} after p_ready(i) (P^T_i in TMEM; the compute warps arrive only once
+    // Q_{i+1} has landed), dK_i and dP^T_{i+1} after ds_ready(i) (dS^T_i in TMEM,
+    // dO_{i+1} landed).  While the issuer waits for one handshake the tensor pipe
+    // runs the burst before it (1024 cycles).  The MMAs of one thread execute in
+    // order: dV_i reads P^T_i before S^T_{i+1} overwrites those columns, and dK_i
+    // reads dS^T_i before dP^T_{i+1} does.  The whole warp runs the schedule and
+    // computes the descriptors; the waits, MMAs and commits are the elected
+    // lane's, so that the compiler issues each MMA as a warp-uniform instruction.
+    uint32_t el_lane;
+    const bool el = elect_one_sync(&el_lane);
     bool ok = true;
     uint32_t nq = 0, it = 0;
     const uint32_t sK = sbase + L::kK;
     const uint32_t sV = sbase + L::kV;
+    auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
+    auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
+    // a wait of the elected lane, its outcome broadcast to the warp
+    auto wait_el = [&](uint64_t* bar, uint32_t parity) {
+      bool w = true;
+      if (el) w = wait_or_abort(bar, parity, ctx, ctl);
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, el_lane) != 0;
+    };
+    // S^T_g = K Q_g^T (c = 0) or dP^T_g = V dO_g^T (c = 1); the second commit
+    // releases this GEMM's read of the Q_g / dO_g stage
+    auto issue_kk = [&](int c, uint32_t g) {
+      const uint64_t a0 = sdesc_sw128(c == 0 ? sK : sV, 16, 1024);
+      const uint64_t b0 = sdesc_sw128(c == 0 ? sq(g) : sdo(g), 16, 1024);
+      const uint32_t d = tmem + (c == 0 ? kColS : kColDP);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+        const uint64_t a = desc_add(a0, off), b = desc_add(b0, off);
+        if (el) mma_bf16(d, a, b, kIdescKK, kk > 0);
+      }
+      if (el) {
+        mma_commit(c == 0 ? &ctl->bar_s_full : &ctl->bar_dp_full);
+        mma_commit(c == 0 ? &ctl->bar_q_empty[g % L::kQStages] : &ctl->bar_do_empty[g % L::kDStages]);
+      }
+    };
+    // dV += P^T dO_g (c = 0; A = P^T in the S^T columns) or dK += dS^T Q_g (c = 1;
+    // A = dS^T in the dP^T columns); the commit releases the dO_g / Q_g stage
+    auto issue_acc = [&](int c, uint32_t g, bool first_acc) {
+      const uint64_t b0 = sdesc_sw128(c == 0 ? sdo(g) : sq(g), kChunkBytes, 1024);
+      const uint32_t d = tmem + (c == 0 ? kColDV : kColDK);
+      const uint32_t a = tmem + (c == 0 ? kColS : kColDP);
+#pragma unroll
+      for (int kk = 0; kk < kBT / 16; ++kk) {
+        const uint64_t b = desc_add(b0, kk * 2048);
+        if (el) mma_bf16_ts(d, a + packed_a_col(kk), b, kIdescKM, (!first_acc || kk > 0) ? 1u : 0u);
+      }
+      if (el) mma_commit(c == 0 ? &ctl->bar_do_empty[g % L::kDStages] : &ctl->bar_q_empty[g % L::kQStages]);
+    };
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
       const Item3 w = decode_item(item, nkt, H);
       if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) continue;
-      if (lane == 0) {
-        auto sq = [&](uint32_t g) { return sbase + L::kQ + (g % L::kQStages) * L::kTileBytes; };
-        auto sdo = [&](uint32_t g) { return sbase + L::kDO + (g % L::kDStages) * L::kTileBytes; };
-        // hand the turn to the other chain (see above)
-        auto pass_turn = [&]() { mbar_arrive(c == 0 ? &ctl->bar_ds_ready : &ctl->bar_p_ready); };
-        // the first GEMM of a chain for query tile g: S^T_g = K Q_g^T or dP^T_g = V dO_g^T;
-        // hands the turn over when `pass` four MMAs before its end (after its first MMA for D = 64)
-        auto issue_first = [&](uint32_t g, bool pass) {
-          const uint64_t a0 = sdesc_sw128(c == 0 ? sK : sV, 16, 1024);
-          const uint64_t b0 = sdesc_sw128(c == 0 ? sq(g) : sdo(g), 16, 1024);
-          const uint32_t d = tmem + (c == 0 ? kColS : kColDP);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_bf16(d, desc_add(a0, off), desc_add(b0, off), kIdescKK, kk > 0);
-            if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
-          }
-          mma_commit(c == 0 ? &ctl->bar_s_full : &ctl->bar_dp_full);
-          // this thread's read of Q_g (chain v) / dO_g (chain k)
-          mma_commit(c == 0 ? &ctl->bar_q_empty[g % L::kQStages] : &ctl->bar_do_empty[g % L::kDStages]);
-        };
-        // the accumulating GEMM of tile g: dV += P^T dO_g (A = P^T in the S^T columns) or
-        // dK += dS^T Q_g (A = dS^T in the dP^T columns)
-        auto issue_acc = [&](uint32_t g, bool first_acc, bool pass) {
-          const uint64_t b0 = sdesc_sw128(c == 0 ? sdo(g) : sq(g), kChunkBytes, 1024);
-          const uint32_t d = tmem + (c == 0 ? kColDV : kColDK);
-          const uint32_t a = tmem + (c == 0 ? kColS : kColDP);
-#pragma unroll
-          for (int kk = 0; kk < kBT / 16; ++kk) {
-            mma_bf16_ts(d, a + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM, (!first_acc || kk > 0) ? 1u : 0u);
-            if (pass && kk == kBT / 16 - 5) pass_turn();
-          }
-          mma_commit(c == 0 ? &ctl->bar_do_empty[g % L::kDStages] : &ctl->bar_q_empty[g % L::kQStages]);
-        };
-        ok = wait_or_abort(&ctl->bar_kv_full, it & 1, ctx, ctl);
-        if (ok) {
-          ok = c == 0 ? wait_or_abort(&ctl->bar_q_full[nq % L::kQStages], (nq / L::kQStages) & 1, ctx, ctl)
-                      : wait_or_abort(&ctl->bar_do_full[nq % L::kDStages], (nq / L::kDStages) & 1, ctx, ctl);
+      ok = wait_el(&ctl->bar_kv_full, it & 1);
+      if (ok) ok = wait_el(&ctl->bar_q_full[nq % L::kQStages], (nq / L::kQStages) & 1);
+      if (ok) ok = wait_el(&ctl->bar_do_full[nq % L::kDStages], (nq / L::kDStages) & 1);
+      if (ok) {
+        tc_fence_after();
+        issue_kk(0, nq);
+        issue_kk(1, nq);
+        if (el) mma_issued = true;
+      }
+      for (int i = 0; ok && i < nqt; ++i) {
+        const uint32_t g = nq + i;
+        const bool more = i + 1 < nqt;
+        if (!(ok = wait_el(&ctl->bar_p_ready, g & 1))) break;
+        if (i == 0 && it > 0) {
+          // the previous item's epilogue must have read dK / dV
+          if (!(ok = wait_el(&ctl->bar_acc_free, (it - 1) & 1))) break;
         }
-        if (ok) {
-          tc_fence_after();
-          // chain k's first burst (dP^T of the item's first tile) releases chain v's first dV burst
-          issue_first(nq, c == 1);
-          mma_issued = true;
-        }
-        // Inside the query loop the compute warps arrive on p_ready / ds_ready only
-        // after they have seen Q_{i+1} / dO_{i+1} land, so no other wait is needed.
-        for (int i = 0; ok && i < nqt; ++i) {
-          const uint32_t g = nq + i;
-          if (!(ok = wait_or_abort(c == 0 ? &ctl->bar_p_ready : &ctl->bar_ds_ready, g & 1, ctx, ctl))) break;
-          if (i == 0 && it > 0) {
-            // the previous item's epilogue must have read dK / dV
-            if (!(ok = wait_or_abort(&ctl->bar_acc_free, (it - 1) & 1, ctx, ctl))) break;
-          }
-          tc_fence_after();
-          const bool more = i + 1 < nqt;
-          // chain v's burst (dV_i, S^T_{i+1}) releases dK_i; chain k's (dK_i, dP^T_{i+1}) releases dV_{i+1}
-          issue_acc(g, i == 0, c == 0 && !more);
-          if (more) issue_first(g + 1, true);
-        }
+        tc_fence_after();
+        issue_acc(0, g, i == 0);
+        if (more) issue_kk(0, g + 1);
+        if (!(ok = wait_el(&ctl->bar_ds_ready, g & 1))) break;
+        tc_fence_after();
+        issue_acc(1, g, i == 0);
+        if (more) issue_kk(1, g + 1);
+      }
+      if (el) {
         if (ok) {
           mma_commit(&ctl->bar_acc_done);
           mma_commit(&ctl->bar_kv_empty);
         } else {
-          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;  // the other issuer waits for our hand-over
+          *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
       nq += nqt;
       ++it;
     }
@@ -529,9 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if ((warp == kMmaWarp || warp == kMmaWarp1) && lane == 0 && mma_issued) {
-    mma_commit(&ctl->bar_final[warp - kMmaWarp]);
-    settle(&ctl->bar_final[warp - kMmaWarp], 0, ctx);
+  if (warp == kMmaWarp && mma_issued) {
+    // every MMA has completed before TMEM is released (mma_issued: the issuing lane)
+    mma_commit(&ctl->bar_final);
+    settle(&ctl->bar_final, 0, ctx);
   }
   if (warp == kProducerWarp && lane == 0) {
     if (kv_armed) settle(&ctl->bar_kv_full, (kv_armed - 1) & 1, ctx);
@@ -568,7 +574,7 @@ struct DqCtl {
   uint64_t bar_qdo_ready;
   uint64_t bar_kv_full[16], bar_kv_empty[16];
   uint64_t bar_s_full, bar_s_read, bar_dp_full, bar_ds_ready;
-  uint64_t bar_dq_done, bar_dq_free, bar_final[2];
+  uint64_t bar_dq_done, bar_dq_free, bar_final[2], bar_dq_step;
   uint32_t tmem_base;
   int abort;
 };
@@ -624,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->bar_ds_ready, kComputeThreads + 1);
     mbar_init(&ctl->bar_dq_done, 1);
     mbar_init(&ctl->bar_dq_free, kComputeThreads);
+    mbar_init(&ctl->bar_dq_step, 1);
     mbar_init(&ctl->bar_final[0], 1);
     mbar_init(&ctl->bar_final[1], 1);
     ctl->abort = 0;
@@ -700,11 +707,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and its turn.  The tensor pipe queues only about one MMA, and a single
     // issuing thread that stopped to wait between GEMMs would leave it idle for
     // a few hundred cycles per wait.  In chain d, dQ_g reads dS_g (in the dP
-    // columns) before dP_{g+1} overwrites them: the MMAs of one thread execute
-    // in order.
+    // columns) as its TMEM A operand, so dP_{g+1}, which overwrites them, is
+    // issued only once dQ_g has completed.
     const int c = warp - kMmaWarp;  // 0: chain s, 1: chain d
     bool ok = true;
     uint32_t g = 0, it = 0;  // g: processed key tiles across items
+    uint32_t dq_step = 0;    // chain d: dQ completions waited for
     auto slot_addr = [&](int slot) { return sbase + L::kRingOff + slot * L::kTileBytes; };
     // hand the turn to the other chain (see above)
     auto pass_turn = [&]() { mbar_arrive(c == 0 ? &ctl->bar_ds_ready : &ctl->bar_s_read); };
@@ -755,7 +763,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int j = next_tile(0);
       if (j >= nkt) {
-        // no attended key: the compute warps write dQ = 0 once dq_done of the item arrives
+        // No attended key: no MMA, and the compute warps write dQ = 0 once dq_done
+        // of the item arrives.  They still store Q and dO and arrive on qdo_ready:
+        // both chains wait for that phase too, or a later item's parity wait could
+        // be satisfied by this phase still being open.
+        if (lane == 0) ok = wait_or_abort(&ctl->bar_qdo_ready, it & 1, ctx, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         if (lane == 0 && c == 1) mma_commit(&ctl->bar_dq_done);
         __syncwarp();
         continue;
@@ -798,7 +812,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
               tc_fence_after();
               issue_dq(g, first, false);
-              if (jn < nkt) issue_dp(g + 1, true);
+              if (jn < nkt) {
+                // dP_{g+1} overwrites the dP columns that dQ_g reads dS from.  An MMA
+                // that takes A from TMEM is not ordered before a later MMA of the same
+                // thread that writes those columns, so dQ_g must complete first.
+                mma_commit(&ctl->bar_dq_step);
+                ok = wait_or_abort(&ctl->bar_dq_step, dq_step & 1, ctx, ctl);
+                ++dq_step;
+                if (ok) {
+                  tc_fence_after();
+                  issue_dp(g + 1, true);
+                }
+              }
             }
           }
         }
@@ -1039,7 +1064,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<grid_k, kThreads, smem, stream>>>(mq, mk, mv, mdo, qd, kd, nl2, delta, mask, mrows,
+    kern<<<grid_k, kSplitThreads, smem, stream>>>(mq, mk, mv, mdo, qd, kd, nl2, delta, mask, mrows,
                                              static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), B, H,
                                              (int)items_k, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;

@@ -12,9 +12,9 @@ constexpr int kBT = 128;  // rows per query tile and per key tile
 constexpr int kChunkBytes = 128 * 128;
 constexpr int kComputeThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;    // first MMA issuer (dK/dV kernel: dV / S^T chain; dQ kernel: S chain)
-constexpr int kMmaWarp1 = 10;  // second MMA issuer (dK/dV kernel: dK / dP^T chain; dQ kernel: dQ / dP chain)
-constexpr int kThreads = 352;
+constexpr int kMmaWarp = 9;    // the MMA issuer (dQ and fused kernels: the first of two)
+constexpr int kMmaWarp1 = 10;  // the second MMA issuer of the dQ and fused kernels
+constexpr int kThreads = 352;  // the dQ and fused kernels' block (the dK/dV kernel uses warps 0-9)
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
