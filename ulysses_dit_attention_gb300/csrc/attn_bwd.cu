@@ -35,10 +35,12 @@
 // Warp roles: warps 0-7 compute (TMEM lane quadrant = warp % 4, column half =
 // warp / 4), warp 8 TMA producer; the dK/dV kernel's tcgen05 issuer is warp 9
 // (one elected lane), the dQ kernel's are warps 9 and 10 (lane 0 of each).
-// MMAs of one thread execute in order; an MMA that reads its A operand from
-// TMEM is not, however, ordered before a later MMA that overwrites those
-// columns (with the A operand in shared memory it is), so the one such pair
-// (dQ_g, then dP_{g+1} in the dQ kernel) is separated by a completion wait.
+// MMAs of one thread execute in order, with one measured exception: an MMA
+// that takes its A operand from TMEM, issued directly behind such an MMA of
+// another GEMM, gave wrong results (dQ_g then dP_{g+1} in the dQ kernel, with
+// or without TMEM columns in common), so that pair is separated by a
+// completion wait.  Consecutive MMAs of one GEMM, and a shared-memory-operand
+// MMA behind a TMEM-operand one, were exact in every run.
 //
 // Query and key sequences are segmented (SeqDesc): a plain (B, S, H, D)
 // tensor is one segment; the sequence shards of a Ulysses step are P segments,
@@ -706,9 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each thread's one wait per burst covers both the compute warps' handshake
     // and its turn.  The tensor pipe queues only about one MMA, and a single
     // issuing thread that stopped to wait between GEMMs would leave it idle for
-    // a few hundred cycles per wait.  In chain d, dQ_g reads dS_g (in the dP
-    // columns) as its TMEM A operand, so dP_{g+1}, which overwrites them, is
-    // issued only once dQ_g has completed.
+    // a few hundred cycles per wait.  In chain d, dQ_g and dP_{g+1} both take A
+    // from TMEM, and dP_{g+1} is issued only once dQ_g has completed (see the
+    // top of this file).
     const int c = warp - kMmaWarp;  // 0: chain s, 1: chain d
     bool ok = true;
     uint32_t g = 0, it = 0;  // g: processed key tiles across items
@@ -813,9 +815,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               issue_dq(g, first, false);
               if (jn < nkt) {
-                // dP_{g+1} overwrites the dP columns that dQ_g reads dS from.  An MMA
-                // that takes A from TMEM is not ordered before a later MMA of the same
-                // thread that writes those columns, so dQ_g must complete first.
+                // dP_{g+1} issued directly behind dQ_g (both with A in TMEM) gave
+                // wrong results, also with dS moved out of the dP columns: dQ_g must
+                // complete first.
                 mma_commit(&ctl->bar_dq_step);
                 ok = wait_or_abort(&ctl->bar_dq_step, dq_step & 1, ctx, ctl);
                 ++dq_step;
