@@ -641,8 +641,29 @@ def run_gpu(args, world, rank, local):
     if fused:
         e2e_step = e2e_step_fused  # noqa: F811
 
+    def host_link():
+        """One step's copies alone (no compute), H2D and D2H concurrently on the two copy
+        streams: the floor the e2e step cannot go below, whatever the overlap."""
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        h2d_s.wait_event(a)
+        d2h_s.wait_event(a)
+        with torch.cuda.stream(h2d_s):
+            for n in ("q", "k", "v", "do"):
+                sh[n].copy_(host[n], non_blocking=True)
+        with torch.cuda.stream(d2h_s):
+            for n, t in (("o", o_sh), ("dq", dq_sh), ("dk", dk_sh), ("dv", dv_sh)):
+                outs_host[n].copy_(t, non_blocking=True)
+        stream.wait_stream(h2d_s)
+        stream.wait_stream(d2h_s)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
     e2e = None
     if not args.no_e2e:
+        link_ms = min(host_link() for _ in range(3))
         e2e_step()
         torch.cuda.synchronize()
         barrier(world)
@@ -662,7 +683,9 @@ def run_gpu(args, world, rank, local):
         d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
         e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "copies": "two copy streams overlapped with compute (event-ordered)"}
+               "copies": "two copy streams overlapped with compute (event-ordered)",
+               "copies_alone_ms_per_step": link_ms,
+               "host_link_gbs": (h2d + d2h) / (link_ms * 1e-3) / 1e9}
     uaa.check_device_status(dev)
 
     pk, src = peaks()
