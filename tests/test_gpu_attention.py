@@ -120,6 +120,23 @@ def test_fully_masked_key_tiles_between_attended_ones(D):
     assert res["o"][0] > 0  # the attended rows were compared against nonzero values
 
 
+@pytest.mark.parametrize("B", [256, 260])
+def test_many_mask_rows(B):
+    """Up to 256 mask rows the forward and the dQ kernel tabulate each row's attended key
+    tiles and skip the others; above that they visit every tile and the masked keys only get
+    P = 0.  Both sides of the limit, with rows whose every key is masked (O = 0, LSE = -inf,
+    no gradients: in the second mode that row goes through the softmax with no attended key)."""
+    S, H, D = 300, 1, 64
+    inp = synth.draw(B, S, H, D, seed=B)
+    pats = ["pxp", "xxa", "xxx", "aap", "xpx"]
+    mask = tile_pattern_mask(B, S, [pats[b % len(pats)] for b in range(B)], seed=B)
+    check_against_oracle(inp, mask, 1.0 / math.sqrt(D), label=f"{B} mask rows")
+    o, lse, dq, dk, dv = run_gpu(inp, 1.0 / math.sqrt(D), mask)
+    empty = [b for b in range(B) if pats[b % len(pats)] == "xxx"]
+    assert (f64(o)[empty] == 0).all() and np.isneginf(f64(lse)[empty]).all()
+    assert (f64(dq)[empty] == 0).all() and (f64(dk)[empty] == 0).all() and (f64(dv)[empty] == 0).all()
+
+
 def test_non_default_scale():
     # scale 0.37 (~3x 1/sqrt(64)) sharpens the softmax; gradients reach |dQ| ~ 6
     inp = synth.draw(1, 200, 2, 64, seed=7)

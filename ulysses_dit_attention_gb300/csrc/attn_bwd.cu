@@ -30,7 +30,9 @@
 //     in bf16.  The extra S / dP recomputation (7 GEMMs instead of 5 for the
 //     whole backward) buys a reduction-free, deterministic dQ.
 // Keys outside the mask get P = 0, hence dK = dV = 0 exactly; key tiles with
-// no attended key are skipped (the dK/dV kernel writes zeros for them).
+// no attended key are skipped (the dK/dV kernel writes zeros for them; the dQ
+// kernel, like the forward, walks a per-mask-row count of attended tiles taken
+// when it starts, up to 256 mask rows, and visits every tile above that).
 //
 // Warp roles: warps 0-7 compute (TMEM lane quadrant = warp % 4, column half =
 // warp / 4), warp 8 TMA producer; the dK/dV kernel's tcgen05 issuer is warp 9
@@ -568,7 +570,9 @@ struct DqLayout {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kRingOff = 0;  // K slots, then V slots (Q and dO live in TMEM)
   static constexpr int kCtl = kRingOff + kRing * kTileBytes;
-  static constexpr int kSmem = kCtl + 512;
+  static constexpr int kWords = kCtl + 512;              // mask bits of the key tile in each K slot
+  static constexpr int kCnt = kWords + kKRing * 16;      // attended key tiles per mask row
+  static constexpr int kSmem = kCnt + kMaxCntRows * 4;
   static_assert(kSmem <= 232448, "dQ shared memory exceeds the per-CTA limit");
 };
 
@@ -648,10 +652,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem_base, 512);
     tmem_relinquish();
   }
+  // Key tiles with at least one attended key, per mask row (batch b uses row b % mrows).
+  // Every role takes an item's tile count from this table, which no one writes after the
+  // start, and only the producer reads the mask itself: it hands each tile's bits to the
+  // compute warps with the tile's K slot (`kwords`), so no per-tile mask read sits on the
+  // issuers' or the compute warps' path.
+  int* tile_cnt = reinterpret_cast<int*>(smem + L::kCnt);
+  uint32_t(*kwords)[4] = reinterpret_cast<uint32_t(*)[4]>(smem + L::kWords);
+  const bool skip = kMask && mrows <= kMaxCntRows;
+  if (skip) {
+    for (int r = threadIdx.x; r < mrows; r += kThreads) tile_cnt[r] = 0;
+    __syncthreads();
+    // one warp per (row, tile) pair, four tiles in flight per warp
+    const int pairs = mrows * nkt;
+    for (int p0 = warp * 4; p0 < pairs; p0 += (kThreads / 32) * 4) {
+      bool any[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pr = p0 + u;
+        bool hit = false;
+        if (pr < pairs) {
+          const int r = pr / nkt, j = pr - r * nkt;
+          const SeqTile kt = seq_tile(kd, j);
+          const uint8_t* row = mask + (size_t)r * kd.total + kd.off[kt.seg] + kt.row0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = 32 * t + lane;
+            hit |= c < kt.valid && row[c] != 0;
+          }
+        }
+        any[u] = hit;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (__any_sync(0xffffffffu, any[u]) && lane == 0 && p0 + u < pairs) atomicAdd(&tile_cnt[(p0 + u) / nkt], 1);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  // key tiles an item of batch b walks
+  auto item_tiles = [&](int b) { return skip ? tile_cnt[b % mrows] : nkt; };
 
   uint32_t kv_armed[16] = {};
   bool mma_issued = false;
@@ -662,12 +704,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n = 0, it = 0, gp = 0;  // n: loads, gp: key tiles loaded
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
+      if (item_tiles(w.b) == 0) continue;  // no attended key: no load, dQ = 0
       SeqCursor kseg;  // key segment cursor (tiles are visited in order)
       for (int j = 0; ok && j < nkt; ++j) {
         uint32_t words[4] = {0u, 0u, 0u, 0u};
         if (kMask) {
           key_tile_bits(mask, kd, w.b % mrows, j, words);
-          if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
+          // the same test as the tile-count table: the other roles expect exactly those tiles
+          if (skip && (words[0] | words[1] | words[2] | words[3]) == 0) continue;
         }
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind, ++n) {  // 0 = K_j, 1 = V_j
@@ -676,6 +720,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && use > 0) ok = wait_or_abort(&ctl->bar_kv_empty[slot], (use - 1) & 1, ctx, ctl);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
+          if (kMask && kind == 0 && lane == 0) {
+            // read by the compute warps between this tile's kv_full and its ds_ready, which
+            // comes before the dQ MMA that frees the slot
+#pragma unroll
+            for (int t = 0; t < 4; ++t) kwords[slot][t] = words[t];
+          }
           if (lane == 0 && (int)n != ctx.drop_load) {
             mbar_arrive_expect_tx(&ctl->bar_kv_full[slot], L::kTileBytes);
             int ms = 0, row0 = j * kBT;
@@ -757,14 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x, ++it) {
       const Item3 w = decode_item(item, nqt, H);
-      // the key tiles of this item, in order (all lanes evaluate the same mask)
-      auto next_tile = [&](int from) {
-        for (int jj = from; jj < nkt; ++jj)
-          if (!kMask || key_tile_any(mask, kd, w.b % mrows, jj)) return jj;
-        return nkt;
-      };
-      int j = next_tile(0);
-      if (j >= nkt) {
+      const int ntl = item_tiles(w.b);  // key tiles of this item
+      if (ntl == 0) {
         // No attended key: no MMA, and the compute warps write dQ = 0 once dq_done
         // of the item arrives.  They still store Q and dO and arrive on qdo_ready:
         // both chains wait for that phase too, or a later item's parity wait could
@@ -795,9 +839,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      bool first = true;
-      while (ok && j < nkt) {
-        const int jn = next_tile(j + 1);
+      for (int i = 0; ok && i < ntl; ++i) {
+        const bool more = i + 1 < ntl;  // another key tile in this item
+        const bool first = i == 0;
         if (lane == 0) {
           if (c == 0) {
             // S of the next key tile once this one's S was read into registers (after the
@@ -805,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_or_abort(&ctl->bar_s_read, g & 1, ctx, ctl);
             if (ok) {
               tc_fence_after();
-              if (jn < nkt) issue_s(g + 1, true);
+              if (more) issue_s(g + 1, true);
               else pass_turn();
             }
           } else {
@@ -814,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
               tc_fence_after();
               issue_dq(g, first, false);
-              if (jn < nkt) {
+              if (more) {
                 // dP_{g+1} issued directly behind dQ_g (both with A in TMEM) gave
                 // wrong results, also with dS moved out of the dP columns: dQ_g must
                 // complete first.
@@ -830,8 +874,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        first = false;
-        j = jn;
         ++g;
       }
       if (!ok) break;
@@ -877,22 +919,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nl2 = nl2g[prow];
       const float dl = delta[prow];
       int ntiles = 0;
+      const int ntl = item_tiles(w.b);  // key tiles of this item
       SeqCursor kseg;  // key segment cursor
-      for (int j = 0; j < nkt; ++j) {
+      for (int j = 0; j < ntl; ++j) {  // j: the key tile itself when there is no mask
         uint32_t words[4];
         if (kMask) {
-          key_tile_bits(mask, kd, w.b % mrows, j, words);
-          if ((words[0] | words[1] | words[2] | words[3]) == 0) continue;
+          // the tile's mask bits, left by the producer with its K slot; the first tile
+          // of an item waits for that slot's load here (later tiles did below)
+          if (j == 0) {
+            ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->bar_kv_full[kslot(g)], kpar(g), ctx, ctl));
+            if (!ok) break;
+          }
+#pragma unroll
+          for (int t = 0; t < 4; ++t) words[t] = kwords[kslot(g)][t];
         }
         // is there a next key tile?  Its K and V are read by the MMAs this tile's
         // s_read and ds_ready release; they normally land long before, and
         // waiting for them here keeps these waits off the issuing thread.
-        bool has_next = j + 1 < nkt;
-        if (kMask) {
-          int jn = j + 1;
-          while (jn < nkt && !key_tile_any(mask, kd, w.b % mrows, jn)) ++jn;
-          has_next = jn < nkt;
-        }
+        const bool has_next = j + 1 < ntl;
         if (has_next) {
           bool okw = wait_or_abort(&ctl->bar_kv_full[kslot(g + 1)], kpar(g + 1), ctx, ctl);
           if (okw) okw = wait_or_abort(&ctl->bar_kv_full[vslot(g + 1)], vpar(g + 1), ctx, ctl);

@@ -62,12 +62,6 @@ constexpr int kExpFmaEvery = 8;
 // arrive, the issuer warp syncs)
 constexpr uint32_t kBarP = 1;
 constexpr uint32_t kBarPCount = 128 + 32;  // log2 units: rescale O only when the max grows by > 2^8
-// With a key mask of at most this many rows, key tiles without an attended key
-// are skipped: their counts per mask row are tabulated in shared memory when the
-// kernel starts (above this many rows every tile is visited and masked keys only
-// get P = 0).
-constexpr int kMaxCntRows = 256;
-
 template <int D>
 struct FwdLayout {
   static constexpr int kRing = 5;

@@ -55,6 +55,11 @@ int check_launch(const char* what);     // cudaGetLastError -> UAA_ERR_CUDA
 // being partial.
 // ----------------------------------------------------------------------------
 constexpr int kMaxSeg = 8;
+// With a key mask of at most this many rows, the forward and the dQ kernel skip
+// key tiles without an attended key: the counts of such tiles per mask row are
+// tabulated in shared memory when the kernel starts (above this many rows every
+// tile is visited and masked keys only get P = 0).
+constexpr int kMaxCntRows = 256;
 struct SeqDesc {
   int nseg;
   int cap;                 // rows per slab
