@@ -21,7 +21,11 @@
  *    head-broadcast (B, 1, 1, S) key-padding mask ("UAA-bwd", Unsupported cases,
  *    per-head masks) and acts as an additive 0 / -inf bias
  *    ("double-transpose", follow-up item 2).  A query row whose keys are all
- *    masked gets O = 0, LSE = -inf and no gradient.
+ *    masked gets O = 0, LSE = -inf and no gradient.  Key tiles (128 keys)
+ *    without an attended key cost no tensor work as long as the mask has at
+ *    most 256 rows (each kernel tabulates the rows' attended tiles when it
+ *    starts); with more rows the forward and the dQ pass compute every tile,
+ *    masked keys at P = 0 (same results).
  *  - All pointers marked "device" are device memory owned by the caller; the
  *    library never allocates or frees device memory.  Host arrays
  *    (shard_lens) are read during the call only.
