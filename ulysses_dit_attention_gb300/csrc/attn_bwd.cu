@@ -179,8 +179,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                          const __grid_constant__ SeqDesc qd, const __grid_constant__ SeqDesc kd,
                          const float* __restrict__ nl2, const float* __restrict__ delta,
                          const uint8_t* __restrict__ key_mask, int mrows, __nv_bfloat16* __restrict__ dk,
-                         __nv_bfloat16* __restrict__ dv, int B, int H, int num_items, float scale,
-                         float scale_log2, DevCtx ctx) {
+                         __nv_bfloat16* __restrict__ dv, int B, int H, int num_items, int head_inner,
+                         float scale, float scale_log2, DevCtx ctx) {
   using L = DkdvLayout<D>;
   constexpr int kChunks = D / 64;
   constexpr uint32_t kIdescKK = idesc_bf16_f32(128, kBT, false, false);  // S^T, dP^T
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     bool ok = true;
     uint32_t nq = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-      const Item3 w = decode_item(item, nkt, H);
+      const Item3 w = head_inner ? decode_item_head_inner(item, nkt, H) : decode_item(item, nkt, H);
       if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) continue;
       if (lane == 0) {
         if (it > 0) ok = wait_or_abort(&ctl->bar_kv_empty, (it - 1) & 1, ctx, ctl);
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       if (el) mma_commit(c == 0 ? &ctl->bar_do_empty[g % L::kDStages] : &ctl->bar_q_empty[g % L::kQStages]);
     };
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-      const Item3 w = decode_item(item, nkt, H);
+      const Item3 w = head_inner ? decode_item_head_inner(item, nkt, H) : decode_item(item, nkt, H);
       if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) continue;
       ok = wait_el(&ctl->bar_kv_full, it & 1);
       if (ok) ok = wait_el(&ctl->bar_q_full[nq % L::kQStages], (nq / L::kQStages) & 1);
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     bool ok = true;
     uint32_t nq = 0, it = 0;
     for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-      const Item3 w = decode_item(item, nkt, H);
+      const Item3 w = head_inner ? decode_item_head_inner(item, nkt, H) : decode_item(item, nkt, H);
       const SeqTile kt = seq_tile(kd, w.t);
       const bool kexists = jrow < kt.valid;  // key row kt.row0 + jrow of segment kt.seg
       const size_t off = seq_elem(kd, B, H, D, w.b, kt.seg, kexists ? kt.row0 + jrow : 0, w.h) + hf * (D / 2);
@@ -1110,9 +1110,12 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* out, con
     const int smem = DkdvLayout<D>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_attn_bwd: smem attribute: %s", cudaGetErrorString(e));
+    // With a key mask, order the items head-innermost (the empty key tiles spread evenly
+    // over the CTAs) when one batch's Q and dO for all heads fit in half of L2
+    const int head_inner = (mask != nullptr && 4LL * H * qd.total * D <= (64LL << 20)) ? 1 : 0;
     kern<<<grid_k, kSplitThreads, smem, stream>>>(mq, mk, mv, mdo, qd, kd, nl2, delta, mask, mrows,
                                              static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), B, H,
-                                             (int)items_k, scale, scale * kLog2e, ctx);
+                                             (int)items_k, head_inner, scale, scale * kLog2e, ctx);
     if ((st = check_launch("uaa_attn_bwd (dK/dV)"))) return st;
   }
   if ((st = record_prof(1, stream))) return st;

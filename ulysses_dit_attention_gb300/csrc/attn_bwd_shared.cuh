@@ -69,6 +69,18 @@ __device__ __forceinline__ Item3 decode_item(int item, int ntiles, int H) {
   it.b = bh / H;
   return it;
 }
+// The same items with the head innermost: (b, t, h).  With a key mask the empty key
+// tiles of a batch (the cheap items) then form runs of H consecutive items, which the
+// round-robin hand-out spreads evenly over the CTAs; the Q / dO streams in flight at
+// once are those of all heads of one batch instead of a few heads.
+__device__ __forceinline__ Item3 decode_item_head_inner(int item, int ntiles, int H) {
+  Item3 it;
+  it.h = item % H;
+  const int bt = item / H;
+  it.t = bt % ntiles;
+  it.b = bt / ntiles;
+  return it;
+}
 
 // TMEM column of the A operand for K step kk (16 elements = 8 packed columns)
 // when the 128 packed K elements sit as two runs of 32 columns at base and
