@@ -66,8 +66,10 @@ typedef enum {
   UAA_ERR_PER_HEAD_MASK = -3, /* a (B, H>1, 1, S) mask: Ulysses cannot shard it ("UAA-bwd",
                                  What does this PR do: fail fast on per-head masks) */
   UAA_ERR_CUDA = -4,          /* a CUDA runtime / driver call failed */
-  UAA_ERR_TIMEOUT = -5        /* a bounded device-side wait ran out (reported by
+  UAA_ERR_TIMEOUT = -5,       /* a bounded device-side wait ran out (reported by
                                  uaa_check_device_status) */
+  UAA_ERR_DEBUG_CHECK = -6    /* debug builds only: a device-side range check failed
+                                 and its access was skipped (uaa_check_device_status) */
 } uaa_status;
 
 /* Attention forward.
@@ -306,7 +308,9 @@ int uaa_assemble_key_mask(const uint8_t* gathered, uint8_t* mask, int P, const i
 
 /* Synchronises `stream`, then reads and clears the library's device status
  * words.  Returns UAA_OK, UAA_ERR_TIMEOUT (a bounded device wait ran out in
- * some kernel since the last check) or UAA_ERR_CUDA. */
+ * some kernel since the last check), UAA_ERR_DEBUG_CHECK (debug builds: a
+ * device-side range check failed; uaa_last_error() names the first one) or
+ * UAA_ERR_CUDA. */
 int uaa_check_device_status(uaa_stream_t stream);
 
 /* Diagnostic for the watchdog: launches one block whose thread waits on an
@@ -335,6 +339,15 @@ const char* uaa_last_error(void);
 
 /* Library version string, e.g. "uaa 0.1 sm_103a". */
 const char* uaa_version(void);
+
+/* 1 for the debug build of the library (libuaa_debug.so, compiled with
+ * -DUAA_DEBUG), 0 otherwise.  The debug build checks, before each access, that
+ * every tensor-core operand lies inside the issuing CTA's shared memory and
+ * TMEM allocation and that every output store of the attention kernels lies
+ * inside its tensor; a failed check skips the access and is reported by
+ * uaa_check_device_status() as UAA_ERR_DEBUG_CHECK.  Same entry points and
+ * results; slower. */
+int uaa_debug_build(void);
 
 #ifdef __cplusplus
 }

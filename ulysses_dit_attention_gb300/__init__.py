@@ -21,17 +21,17 @@ import threading
 
 import torch
 
-from .build import LIB_PATH
+from .build import DEBUG_LIB_PATH, LIB_PATH
 
 __all__ = [
     "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_fused_workspace_bytes", "seq_to_head", "head_to_seq",
     "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms", "debug_drop_load",
     "set_bwd_profile_events", "Attention", "attn_fwd_groups", "attn_bwd_groups",
-    "attention", "UlyssesAttention", "ulysses_attention", "STATUS",
+    "attention", "UlyssesAttention", "ulysses_attention", "STATUS", "debug_build",
 ]
 
 STATUS = {0: "UAA_OK", -1: "UAA_ERR_INVALID_ARG", -2: "UAA_ERR_UNSUPPORTED", -3: "UAA_ERR_PER_HEAD_MASK",
-          -4: "UAA_ERR_CUDA", -5: "UAA_ERR_TIMEOUT"}
+          -4: "UAA_ERR_CUDA", -5: "UAA_ERR_TIMEOUT", -6: "UAA_ERR_DEBUG_CHECK"}
 
 
 class UAAError(RuntimeError):
@@ -75,19 +75,24 @@ _SIGS = {
     "uaa_set_bwd_profile_events": (None, [_P, _P, _P]),
     "uaa_last_error": (ctypes.c_char_p, []),
     "uaa_version": (ctypes.c_char_p, []),
+    "uaa_debug_build": (_I, []),
 }
 
 
 def lib():
-    """Load ``libuaa.so`` (once).  Raises if it has not been built."""
+    """Load ``libuaa.so`` (once; ``libuaa_debug.so``, the build with device range checks,
+    when the environment sets ``UAA_DEBUG=1``).  Raises if it has not been built."""
     global _lib
     if _lib is None:
         with _lib_lock:
             if _lib is None:
-                if not os.path.exists(LIB_PATH):
-                    raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                                       "`python -m ulysses_dit_attention_gb300.build` (no fallback exists)")
-                handle = ctypes.CDLL(LIB_PATH)
+                debug = os.environ.get("UAA_DEBUG", "") == "1"
+                path = DEBUG_LIB_PATH if debug else LIB_PATH
+                if not os.path.exists(path):
+                    how = "--debug " if debug else ""
+                    raise RuntimeError(f"{path} is missing: build it with "
+                                       f"`python -m ulysses_dit_attention_gb300.build {how}` (no fallback exists)")
+                handle = ctypes.CDLL(path)
                 for name, (res, args) in _SIGS.items():
                     fn = getattr(handle, name)
                     fn.restype = res
@@ -382,6 +387,11 @@ def assemble_key_mask(gathered, shard_lens, out=None):
         out = torch.empty((B, sum(lens)), dtype=torch.uint8, device=gathered.device)
     _check(lib().uaa_assemble_key_mask(_ptr(gathered), _ptr(out), P, arr, cap, B, _P(_stream(gathered.device))))
     return out
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the debug build (device range checks)."""
+    return bool(lib().uaa_debug_build())
 
 
 def check_device_status(device=None):

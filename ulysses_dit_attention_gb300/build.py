@@ -3,7 +3,10 @@
 Each ``csrc/*.cu`` file is compiled to an object in parallel, then the objects
 are linked into ``ulysses_dit_attention_gb300/libuaa.so`` with the static CUDA
 runtime.  A rebuild is skipped when the library is newer than every source.
-Usage: ``python -m ulysses_dit_attention_gb300.build [--force]``.
+``debug=True`` builds ``libuaa_debug.so`` instead, with ``-DUAA_DEBUG``: the
+kernels then range-check their tensor-core operands and output stores (the
+binding loads it when ``UAA_DEBUG=1``).
+Usage: ``python -m ulysses_dit_attention_gb300.build [--force] [--debug]``.
 """
 from __future__ import annotations
 
@@ -20,6 +23,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libuaa.so")
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG, "libuaa_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
@@ -41,22 +46,24 @@ def _deps():
         os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    os.makedirs(build_dir, exist_ok=True)
+    flags = NVCC_FLAGS + (["-DUAA_DEBUG"] if debug else []) + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,14 +75,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lrt", "-lpthread", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libuaa.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        raise RuntimeError(f"link of {os.path.basename(lib_path)} failed:\n{r.stderr}")
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -244,6 +244,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  const MmaGuard mg = mma_guard(ctx, sbase, L::kSmem, tmem, 512);  // debug builds' operand checks
+  const size_t k_extent = seq_extent(kd, B, H, D);
 
   uint32_t q_armed[3] = {0, 0, 0}, do_armed[2] = {0, 0}, kv_armed = 0;
   bool mma_issued = false;
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
         const uint64_t a = desc_add(a0, off), b = desc_add(b0, off);
-        if (el) mma_bf16(d, a, b, kIdescKK, kk > 0);
+        if (el) mma_ss_checked(mg, d, a, b, kIdescKK, kk > 0, kBT);
       }
       if (el) {
         mma_commit(c == 0 ? &ctl->bar_s_full : &ctl->bar_dp_full);
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kBT / 16; ++kk) {
         const uint64_t b = desc_add(b0, kk * 2048);
-        if (el) mma_bf16_ts(d, a + packed_a_col(kk), b, kIdescKM, (!first_acc || kk > 0) ? 1u : 0u);
+        if (el) mma_ts_checked(mg, d, a + packed_a_col(kk), b, kIdescKM, (!first_acc || kk > 0) ? 1u : 0u, D);
       }
       if (el) mma_commit(c == 0 ? &ctl->bar_do_empty[g % L::kDStages] : &ctl->bar_q_empty[g % L::kQStages]);
     };
@@ -415,9 +417,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       const SeqTile kt = seq_tile(kd, w.t);
       const bool kexists = jrow < kt.valid;  // key row kt.row0 + jrow of segment kt.seg
       const size_t off = seq_elem(kd, B, H, D, w.b, kt.seg, kexists ? kt.row0 + jrow : 0, w.h) + hf * (D / 2);
+      const bool kstore = kexists && guard_store(ctx, off, D / 2, k_extent);  // this thread's half row of dK, dV
       if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) {
         // no attended key in this tile: dK = dV = 0
-        if (kexists) {
+        if (kstore) {
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             *reinterpret_cast<uint4*>(dk + off + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
         tmem_ld32(tl + kColDV + hf * (D / 2) + 32 * c, gg);
-        if (kexists) {
+        if (kstore) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           }
         }
         tmem_ld32(tl + kColDK + hf * (D / 2) + 32 * c, gg);
-        if (kexists) {
+        if (kstore) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -692,6 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  const MmaGuard mg = mma_guard(ctx, sbase, L::kSmem, tmem, 512);  // debug builds' operand checks
+  const size_t q_extent = seq_extent(qd, B, H, D);
   // key tiles an item of batch b walks
   auto item_tiles = [&](int b) { return skip ? tile_cnt[b % mrows] : nkt; };
 
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-        mma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
+        mma_ts_checked(mg, tmem + kColS, tmem + kColQ + kk * 8, desc_add(b0, off), kIdescKK, kk > 0, kBT);
         if (pass && kk == (D / 16 > 4 ? D / 16 - 5 : 0)) pass_turn();
       }
       mma_commit(&ctl->bar_s_full);
@@ -788,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-        mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, desc_add(b0, off), kIdescKK, kk > 0);
+        mma_ts_checked(mg, tmem + kColDP, tmem + kColDO + kk * 8, desc_add(b0, off), kIdescKK, kk > 0, kBT);
       }
       if (pass) pass_turn();
       mma_commit(&ctl->bar_dp_full);
@@ -799,8 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b0 = sdesc_sw128(slot_addr(kslot(gg)), kChunkBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < kBT / 16; ++kk) {
-        mma_bf16_ts(tmem + kColDQ, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
-                    (!first || kk > 0) ? 1u : 0u);
+        mma_ts_checked(mg, tmem + kColDQ, tmem + kColDP + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
+                       (!first || kk > 0) ? 1u : 0u, D);
         if (pass && kk == kBT / 16 - 5) pass_turn();
       }
       mma_commit(&ctl->bar_kv_empty[kslot(gg)]);
@@ -1006,6 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       __nv_bfloat16* drow = dq + qoff + hf * (D / 2);
+      const bool qstore = qvalid && guard_store(ctx, qoff + hf * (D / 2), D / 2, q_extent);  // this thread's half row
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
@@ -1014,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 32; ++t) gg[t] = 0.f;
         }
-        if (qvalid) {
+        if (qstore) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;

@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  const MmaGuard mg = mma_guard(ctx, sbase, L::kSmem, tmem, 512);  // debug builds' operand checks
+  const size_t k_extent = (size_t)B * Sk * H * D, acc_extent = (size_t)B * H * nqt * kBT * D;
 
   uint32_t q_armed[4] = {0, 0, 0, 0}, do_armed[4] = {0, 0, 0, 0}, kv_armed = 0;
   bool mma_issued = false;
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_bf16(d, desc_add(a0, off), desc_add(b0, off), kIdescKK, kk > 0);
+            mma_ss_checked(mg, d, desc_add(a0, off), desc_add(b0, off), kIdescKK, kk > 0, kBT);
           }
           mma_commit(isA ? &ctl->bar_s_full : &ctl->bar_dp_full);
           mma_commit(isA ? &ctl->bar_q_empty[g % NS] : &ctl->bar_do_empty[g % NS]);
@@ -241,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a = tmem + (isA ? kColS : kColDP);
 #pragma unroll
           for (int kk = 0; kk < kBT / 16; ++kk)
-            mma_bf16_ts(d, a + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM, (!first_acc || kk > 0) ? 1u : 0u);
+            mma_ts_checked(mg, d, a + packed_a_col(kk), desc_add(b0, kk * 2048), kIdescKM,
+                           (!first_acc || kk > 0) ? 1u : 0u, D);
           mma_commit(isA ? &ctl->bar_do_empty[g % NS] : &ctl->bar_q_empty[g % NS]);
         };
         // D = 128: dQ_g^T = K^T dS_g^T, so that a TMEM lane holds one dQ column d for the
@@ -256,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a0 = kTransDq ? k0 : ds0, b0 = kTransDq ? ds0 : k0;
 #pragma unroll
           for (int kk = 0; kk < kBT / 16; ++kk)
-            mma_bf16(tmem + kColDQ, desc_add(a0, kk * 2048), desc_add(b0, kk * 2048), kIdescQ, kk > 0);
+            mma_ss_checked(mg, tmem + kColDQ, desc_add(a0, kk * 2048), desc_add(b0, kk * 2048), kIdescQ, kk > 0,
+                           kTransDq ? kBT : D);
           mma_commit(&ctl->bar_dq_full);
         };
         ok = wait_or_abort(&ctl->bar_kv_full, it & 1, ctx, ctl);
@@ -333,9 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kvalid_rows = Sk - w.t * kBT < kBT ? Sk - w.t * kBT : kBT;
       const bool kexists = jrow < kvalid_rows;
       const size_t off = (((size_t)w.b * Sk + (kexists ? w.t * kBT + jrow : 0)) * H + w.h) * D + hf * (D / 2);
+      const bool kstore = kexists && guard_store(ctx, off, D / 2, k_extent);  // this thread's half row of dK, dV
       if (kMask && !key_tile_any(mask, kd, w.b % mrows, w.t)) {
         // no attended key in this tile: dK = dV = 0, and no dQ contribution
-        if (kexists) {
+        if (kstore) {
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             *reinterpret_cast<uint4*>(dk + off + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
@@ -426,12 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // lane = column d = jrow, acc[c] = dQ[query 64*hf + c][d]: the warp adds 32 consecutive
             // columns of one query row per instruction
             const int q0 = qt * kBT + 64 * hf;
+            const size_t a0 = ((size_t)w.b * H + w.h) * ((size_t)nqt * kBT) * D + (size_t)q0 * D + jrow;
+            if (guard_store(ctx, a0, (size_t)63 * D + 1, acc_extent)) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (q0 + c < Sq) atomicAdd(acc_bh + (size_t)(q0 + c) * D + jrow, acc[c]);
+              for (int c = 0; c < 64; ++c)
+                if (q0 + c < Sq) atomicAdd(acc_bh + (size_t)(q0 + c) * D + jrow, acc[c]);
+            }
           } else {
             const int qrow = qt * kBT + jrow;  // query row of this thread in dQ_g
-            if (qrow < Sq) {
+            if (qrow < Sq &&
+                guard_store(ctx, ((size_t)w.b * H + w.h) * ((size_t)nqt * kBT) * D + (size_t)qrow * D + hf * (D / 2),
+                            D / 2, acc_extent)) {
               float* dst = acc_bh + (size_t)qrow * D + hf * (D / 2);
 #pragma unroll
               for (int c = 0; c < D / 8; ++c)
@@ -451,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 64; ++c) {
         float gg[32];
         tmem_ld32(tl + kColDV + hf * (D / 2) + 32 * c, gg);
-        if (kexists) {
+        if (kstore) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_ld32(tl + kColDK + hf * (D / 2) + 32 * c, gg);
-        if (kexists) {
+        if (kstore) {
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 v;

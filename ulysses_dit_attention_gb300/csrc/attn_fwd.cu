@@ -211,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  const MmaGuard mg = mma_guard(ctx, sbase, L::kSmem, tmem, 512);  // debug builds' operand checks
+  const size_t o_extent = seq_extent(qd, B, H, D), lse_extent = (size_t)B * H * qd.total;
   // key tiles an item of batch b walks
   auto item_tiles = [&](int b) { return skip ? tile_cnt[b % mrows] : nkt; };
 
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
         const uint64_t a = desc_add(dq0, off), b = desc_add(dk0, off);
-        if (el) mma_bf16(d, a, b, kIdescS, kk > 0);
+        if (el) mma_ss_checked(mg, d, a, b, kIdescS, kk > 0, kBN);
       }
       if (el) mma_commit(&ctl->bar_s_full[t]);
     };
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
         const uint64_t b = desc_add(dv0, kk * 2048);
-        if (el) mma_bf16_ts(d, aP + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        if (el) mma_ts_checked(mg, d, aP + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u, D);
       }
       if (el) mma_commit(&ctl->bar_pv_done[t]);
     };
@@ -415,10 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const SeqTile qt = seq_tile(qd, 2 * w.qp + t);
         if (row < qt.valid) {
           const int qs = qt.row0 + row;
-          __nv_bfloat16* orow = out + seq_elem(qd, B, H, D, w.b, qt.seg, qs, w.h);
+          const size_t oo = seq_elem(qd, B, H, D, w.b, qt.seg, qs, w.h);
+          if (guard_store(ctx, oo, D, o_extent)) {
+            __nv_bfloat16* orow = out + oo;
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
-          lse[((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs] = -INFINITY;
+            for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          const size_t lo = ((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs;
+          if (guard_store(ctx, lo, 1, lse_extent)) lse[lo] = -INFINITY;
         }
         continue;
       }
@@ -531,12 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool qvalid = row < qt.valid;
       const int qs = qt.row0 + row;  // row within the query segment
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = out + seq_elem(qd, B, H, D, w.b, qt.seg, qvalid ? qs : 0, w.h);
+      const size_t oo = seq_elem(qd, B, H, D, w.b, qt.seg, qvalid ? qs : 0, w.h);
+      const bool ostore = qvalid && guard_store(ctx, oo, D, o_extent);
+      __nv_bfloat16* orow = out + oo;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         tmem_ld32(tl + colO + 32 * c, o);
-        if (qvalid) {
+        if (ostore) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 v;
@@ -550,8 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&ctl->bar_o_free);
-      if (qvalid)
-        lse[((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
+      if (qvalid) {
+        const size_t lo = ((size_t)w.b * H + w.h) * qd.total + qd.off[qt.seg] + qs;
+        if (guard_store(ctx, lo, 1, lse_extent)) lse[lo] = l_run > 0.f ? mu * kLn2 + logf(l_run) : -INFINITY;
+      }
       g += nt;
     }
   }

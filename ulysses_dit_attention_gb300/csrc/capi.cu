@@ -15,10 +15,11 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
-// The status words: one pair per device (sticky status bits, epoch of the last
-// call that gave up), a file-scope device variable of this translation unit.
-// Its device address is looked up once per device.
-__device__ unsigned int g_status_word[2];
+// The status words of a device: sticky status bits, epoch of the last call that
+// gave up, and (debug builds) the first failed range check and its value; a
+// file-scope device variable of this translation unit.  Its device address is
+// looked up once per device.
+__device__ unsigned int g_status_word[4];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -165,7 +166,13 @@ extern "C" {
 
 const char* uaa_last_error(void) { return g_last_error; }
 
+#ifdef UAA_DEBUG
+const char* uaa_version(void) { return "uaa 0.1 sm_103a (debug: device range checks)"; }
+int uaa_debug_build(void) { return 1; }
+#else
 const char* uaa_version(void) { return "uaa 0.1 sm_103a"; }
+int uaa_debug_build(void) { return 0; }
+#endif
 
 void uaa_set_wait_timeout_ms(unsigned int ms) {
   g_timeout_ns.store(ms ? (unsigned long long)ms * 1000ull * 1000ull : kDefaultTimeoutNs);
@@ -180,9 +187,12 @@ int uaa_check_device_status(uaa_stream_t stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
-  unsigned int word = 0;  // the sticky bits; the abort epoch needs no clearing (an epoch recurs only after 2^32 calls)
-  e = cudaMemcpy(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost);
+  // [0] the sticky bits; [1] the abort epoch, which needs no clearing (an epoch recurs only
+  // after 2^32 calls); [2], [3] the first failed debug check (rewritten by the next first one)
+  unsigned int words[4] = {0u, 0u, 0u, 0u};
+  e = cudaMemcpy(words, ctx.status, sizeof(words), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  const unsigned int word = words[0];
   if (word) {
     e = cudaMemset(ctx.status, 0, sizeof(unsigned int));
     if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
@@ -193,6 +203,12 @@ int uaa_check_device_status(uaa_stream_t stream) {
     return set_error(UAA_ERR_TIMEOUT, "a bounded device-side wait ran out (status word 0x%x)", word);
   if (word & kStatusBadLaunch)
     return set_error(UAA_ERR_CUDA, "a kernel refused its launch configuration (status word 0x%x)", word);
+  if (word & kStatusDebugCheck) {
+    static const char* what[4] = {"?", "MMA shared-memory operand outside the CTA's shared memory",
+                                  "MMA TMEM address outside the CTA's allocation", "output store past the tensor end"};
+    return set_error(UAA_ERR_DEBUG_CHECK, "a device range check failed and its access was skipped: %s (value 0x%x)",
+                     what[words[2] < 4 ? words[2] : 0], words[3]);
+  }
   return UAA_OK;
 }
 

@@ -21,6 +21,14 @@ namespace uaa {
 enum : uint32_t {
   kStatusTimeout = 1u,      // a bounded wait ran out
   kStatusBadLaunch = 2u,    // a kernel refused its launch configuration (e.g. misaligned shared memory)
+  kStatusDebugCheck = 4u,   // debug builds (UAA_DEBUG): a device-side range check failed, the access was skipped
+};
+// Debug builds leave the first failed check in status[2] (kDbg* below) and its
+// offending value in status[3].
+enum : uint32_t {
+  kDbgSmemOperand = 1u,  // an MMA shared-memory descriptor starts outside this CTA's dynamic shared memory
+  kDbgTmemAddress = 2u,  // an MMA accumulator / TMEM operand lies outside the CTA's TMEM allocation
+  kDbgGlobalStore = 3u,  // an output store lies past the end of its tensor
 };
 
 // Launch context handed to every kernel.  status[0] holds the sticky status
@@ -293,6 +301,120 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// ----------------------------------------------------------------------------
+// Range checks of debug builds (compiled with -DUAA_DEBUG; a separate library).
+// Every MMA's operands are checked before it is issued -- shared-memory
+// descriptors must start inside this CTA's dynamic shared memory with room for a
+// 1 KB swizzle atom, accumulators and TMEM A operands must lie inside the CTA's
+// TMEM columns -- and every output store of the attention kernels against the end
+// of its tensor.  A failed check skips the access and sets kStatusDebugCheck (the
+// first failure also records what and where, see kDbg*).  Release builds compile
+// the checks away: the guard structs are empty and every guard is `true`.
+// ----------------------------------------------------------------------------
+struct MmaGuard {
+#ifdef UAA_DEBUG
+  unsigned int* status;
+  uint32_t smem_lo, smem_hi;  // [first, last + 1) shared-window byte address of the dynamic shared memory
+  uint32_t tcol_lo, tcol_hi;  // allocated TMEM columns
+#endif
+};
+
+__device__ __forceinline__ void dbg_fail(unsigned int* status, uint32_t what, uint32_t value) {
+#ifdef UAA_DEBUG
+  if (!(atomicOr(status, kStatusDebugCheck) & kStatusDebugCheck)) {
+    atomicExch(status + 2, what);
+    atomicExch(status + 3, value);
+  }
+#else
+  (void)status;
+  (void)what;
+  (void)value;
+#endif
+}
+
+__device__ __forceinline__ MmaGuard mma_guard(const DevCtx& ctx, uint32_t sbase, uint32_t smem_bytes,
+                                              uint32_t tmem, uint32_t tcols) {
+  MmaGuard g;
+#ifdef UAA_DEBUG
+  g.status = ctx.status;
+  g.smem_lo = sbase;
+  g.smem_hi = sbase + smem_bytes;
+  g.tcol_lo = tmem & 0xFFFFu;
+  g.tcol_hi = (tmem & 0xFFFFu) + tcols;
+#else
+  (void)ctx;
+  (void)sbase;
+  (void)smem_bytes;
+  (void)tmem;
+  (void)tcols;
+#endif
+  return g;
+}
+
+__device__ __forceinline__ bool guard_smem(const MmaGuard& g, uint64_t desc) {
+#ifdef UAA_DEBUG
+  const uint32_t a = (uint32_t)(desc & 0x3FFFull) << 4;
+  if (a < g.smem_lo || a + 1024u > g.smem_hi) {
+    dbg_fail(g.status, kDbgSmemOperand, a);
+    return false;
+  }
+#else
+  (void)g;
+  (void)desc;
+#endif
+  return true;
+}
+
+// ncols TMEM columns from `taddr` (lane field 0: all 128 lanes)
+__device__ __forceinline__ bool guard_tmem(const MmaGuard& g, uint32_t taddr, uint32_t ncols) {
+#ifdef UAA_DEBUG
+  const uint32_t col = taddr & 0xFFFFu;
+  if ((taddr >> 16) != 0u || col < g.tcol_lo || col + ncols > g.tcol_hi) {
+    dbg_fail(g.status, kDbgTmemAddress, taddr);
+    return false;
+  }
+#else
+  (void)g;
+  (void)taddr;
+  (void)ncols;
+#endif
+  return true;
+}
+
+// The MMAs with their debug checks: M = 128, N = n accumulator columns.
+__device__ __forceinline__ void mma_ss_checked(const MmaGuard& g, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate, uint32_t n) {
+  if (guard_tmem(g, d_tmem, n) && guard_smem(g, adesc) && guard_smem(g, bdesc))
+    mma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+}
+// A in TMEM: 128 lanes x 16 bf16 = 8 packed columns
+__device__ __forceinline__ void mma_ts_checked(const MmaGuard& g, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate, uint32_t n) {
+  if (guard_tmem(g, d_tmem, n) && guard_tmem(g, a_tmem, 8u) && guard_smem(g, bdesc))
+    mma_bf16_ts(d_tmem, a_tmem, bdesc, idesc, accumulate);
+}
+
+// An output store of `n` elements at element offset `off` of a tensor of `extent` elements.
+__device__ __forceinline__ bool guard_store(const DevCtx& ctx, size_t off, size_t n, size_t extent) {
+#ifdef UAA_DEBUG
+  if (off + n > extent) {
+    dbg_fail(ctx.status, kDbgGlobalStore, (uint32_t)(off > 0xFFFFFFFFull ? 0xFFFFFFFFull : off));
+    return false;
+  }
+#else
+  (void)ctx;
+  (void)off;
+  (void)n;
+  (void)extent;
+#endif
+  return true;
+}
+
+// Elements of a (nseg*B, cap, H, D) sequence buffer (plain BSHD: B*S*H*D).
+__host__ __device__ __forceinline__ size_t seq_extent(const SeqDesc& sd, int B, int H, int D) {
+  return (size_t)sd.nseg * B * sd.cap * H * D;
 }
 
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this thread has completed.
