@@ -369,9 +369,8 @@ def run_configs(uaa, args, dev, local):
     with Clocks(local) as clk:
         for name in PER_CONFIG:
             w = synth.workload(name)
-            big = w.S * w.S * w.H * w.B > (1 << 32)
-            recs[name] = time_config(uaa, w, dev, warmup=3 if big else 10, iters=5 if big else 30,
-                                     fused_bwd=args.bwd == "fused")
+            # 10 warm-up and 50 timed replays of each graph, the median reported
+            recs[name] = time_config(uaa, w, dev, warmup=10, iters=50, fused_bwd=args.bwd == "fused")
     for name in PER_CONFIG:
         w = synth.workload(name)
         r = recs[name]
