@@ -125,10 +125,11 @@ class Clocks:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "power_w": statistics.median(pw) if pw else None}
 
 
 def dist_setup(n_gpus):
@@ -668,15 +669,16 @@ def run_gpu(args, world, rank, local):
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        h2d_s.wait_event(e0)
-        d2h_s.wait_event(e0)
-        for _ in range(args.steps):
-            e2e_step()
-        stream.wait_stream(h2d_s)
-        stream.wait_stream(d2h_s)
-        e1.record(stream)
-        torch.cuda.synchronize()
+        with Clocks(local) as clk_e2e:  # this loop follows the device-timed one on a warm GPU
+            e0.record(stream)
+            h2d_s.wait_event(e0)
+            d2h_s.wait_event(e0)
+            for _ in range(args.steps):
+                e2e_step()
+            stream.wait_stream(h2d_s)
+            stream.wait_stream(d2h_s)
+            e1.record(stream)
+            torch.cuda.synchronize()
         e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
@@ -684,7 +686,8 @@ def run_gpu(args, world, rank, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "copies": "two copy streams overlapped with compute (event-ordered)",
                "copies_alone_ms_per_step": link_ms,
-               "host_link_gbs": (h2d + d2h) / (link_ms * 1e-3) / 1e9}
+               "host_link_gbs": (h2d + d2h) / (link_ms * 1e-3) / 1e9,
+               "clocks": clk_e2e.summary()}
     uaa.check_device_status(dev)
 
     pk, src = peaks()
