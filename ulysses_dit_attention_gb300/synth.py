@@ -88,6 +88,19 @@ def draw(B, S, H, D, seed, masked=False, with_grad_out=True):
     return out
 
 
+def draw_device(B, S, H, D, seed, device):
+    """The same recipe drawn by a seeded generator on ``device`` (for tensors too large to draw
+    on the host in reasonable time): bf16 ``q, k, v, do`` of shape ``(B, S, H, D)``, drawn one
+    after the other, each as fp32 N(0, 1) rounded to bf16.  A different random stream from
+    :func:`draw` for the same seed."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = {}
+    for n in ("q", "k", "v", "do"):
+        out[n] = torch.randn((B, S, H, D), generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+    return out
+
+
 def make(w: Workload, with_grad_out=True):
     return draw(w.B, w.S, w.H, w.D, w.seed, w.masked, with_grad_out)
 
