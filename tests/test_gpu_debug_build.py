@@ -8,8 +8,8 @@ access and makes ``check_device_status()`` raise UAA_ERR_DEBUG_CHECK.  This test
 builds that library and re-runs the edge-case GPU tests -- ragged and single-row
 tiles, interior and trailing masked key tiles, keyless batches, more than 256
 mask rows, Sq != Sk, grouped launches, the masked exchange path, the fused
-exchanges over uneven and empty shards, the one-pass backward and the canary
-guard bands -- in a child process that loads it: each of those tests checks the
+exchanges over uneven and empty shards, the one-pass backward, the canary
+guard bands and tensors past 2^31 elements -- in a child process that loads it: each of those tests checks the
 device status after its calls, so any failed check fails it, and their parity
 checks must hold as in the release build.
 """
@@ -33,6 +33,7 @@ CHILD_SELECTION = [
     "tests/test_gpu_fused_ulysses.py",
     "tests/test_gpu_fused_backward.py",
     "tests/test_gpu_guard_bands.py",
+    "tests/test_gpu_large_offsets.py",
 ]
 # the full-size workloads (sampled heads of S = 27280 and S = 4096) are left to the release run:
 # they exercise the same kernels on more items, not other addressing
