@@ -9,9 +9,9 @@ builds that library and re-runs the edge-case GPU tests -- ragged and single-row
 tiles, interior and trailing masked key tiles, keyless batches, more than 256
 mask rows, Sq != Sk, grouped launches, the masked exchange path, the fused
 exchanges over uneven and empty shards, the one-pass backward, the canary
-guard bands and tensors past 2^31 elements -- in a child process that loads it: each of those tests checks the
-device status after its calls, so any failed check fails it, and their parity
-checks must hold as in the release build.
+guard bands and tensors past 2^31 elements -- in a child process that loads
+it: each of those tests checks the device status after its calls, so any failed
+check fails it, and their parity checks must hold as in the release build.
 """
 import os
 import re
