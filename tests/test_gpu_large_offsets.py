@@ -7,6 +7,9 @@ device by the seeded generator of the input module:
   D = 128, with a key-padding mask: (b, h) problems are independent, so the oracle
   checks whole problems -- O, LSE, dQ, dK, dV -- at the start, in the middle and at
   the very end of the tensors, where element offsets exceed 2^31;
+* the Ulysses re-layouts of four uneven shards of such a sequence: seq->head must equal
+  plain slicing of the concatenated sequence and head->seq must restore the shards,
+  bit for bit;
 * one long sequence, B = 1, S = 131072, H = 136, D = 128: the oracle checks O, LSE
   and dQ on query-row blocks at both ends of the sequence for the first and the last
   head (each row against all keys); dK and dV, which need every query per key, are
@@ -102,4 +105,31 @@ def test_long_sequence_past_2_31_elements():
     dk_abs = float(dk.float().abs().sum(dim=1).max())
     assert dk_sum <= 1e-3 * dk_abs, f"sum_j dK_j = {dk_sum:.3e} against sum_j |dK_j| = {dk_abs:.3e}"
     del inp, q, k, v, do, o, lse, dq, dk, dv
+    _release()
+
+
+def test_relayouts_past_2_31_elements():
+    lens, B, H, D = [32770, 32768, 32767, 32767], 1, 136, 128
+    P, cap, N = len(lens), max(lens), sum(lens)
+    assert P * B * cap * H * D > 2 ** 31
+    g = torch.Generator(device=DEV).manual_seed(41)
+    x = torch.randint(-30000, 30000, (P, B, cap, H, D), generator=g, device=DEV, dtype=torch.int16)
+    x = x.view(torch.bfloat16)  # arbitrary bit patterns: the re-layouts move bytes
+    y = uaa.seq_to_head(x, lens)
+    uaa.check_device_status()
+    Hg = H // P
+    assert y.shape == (P, B, N, Hg, D)
+    off = 0
+    for p, L in enumerate(lens):
+        for grp in (0, P - 1):
+            want = x[p, :, :L, grp * Hg:(grp + 1) * Hg].view(torch.int16)
+            assert torch.equal(y[grp, :, off:off + L].view(torch.int16), want), f"shard {p} group {grp}"
+        off += L
+    back = torch.full_like(x, float("nan"))
+    uaa.head_to_seq(y, lens, cap, out=back)
+    uaa.check_device_status()
+    for p, L in enumerate(lens):
+        assert torch.equal(back[p, :, :L].view(torch.int16), x[p, :, :L].view(torch.int16)), f"shard {p}"
+        assert bool((back[p, :, L:].view(torch.int16) == 0).all()), f"padding rows of shard {p}"
+    del x, y, back
     _release()
