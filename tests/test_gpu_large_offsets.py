@@ -1,20 +1,21 @@
 """Tensors past 2^31 elements: every kernel must address them with 64-bit offsets.
 
-Two shapes, each with 2.2-2.3e9 elements per tensor (4.5 GB in bf16), drawn on the
-device by the seeded generator of the input module:
+Each case has 2.2-2.3e9 elements per tensor (4.5 GB in bf16), drawn on the device
+by the seeded generator of the input module:
 
-* many short problems, B = 640, S = 200 (two tiles, the second ragged), H = 136,
-  D = 128, with a key-padding mask: (b, h) problems are independent, so the oracle
-  checks whole problems -- O, LSE, dQ, dK, dV -- at the start, in the middle and at
-  the very end of the tensors, where element offsets exceed 2^31;
-* the Ulysses re-layouts of four uneven shards of such a sequence: seq->head must equal
-  plain slicing of the concatenated sequence and head->seq must restore the shards,
-  bit for bit;
-* one long sequence, B = 1, S = 131072, H = 136, D = 128: the oracle checks O, LSE
-  and dQ on query-row blocks at both ends of the sequence for the first and the last
-  head (each row against all keys); dK and dV, which need every query per key, are
-  checked through the identities sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 and
-  through buffers filled with NaN before the call (every row must be written).
+* many short problems, B = 640, S = 200 (two tiles, the second ragged), H = 136 at
+  D = 128 (272 at D = 64), with a key-padding mask: (b, h) problems are independent,
+  so the oracle checks whole problems -- O, LSE, dQ, dK, dV -- at the start, in the
+  middle and at the very end of the tensors, where element offsets exceed 2^31;
+* one long sequence, B = 1, S = 131072, H = 136 at D = 128 (272 at D = 64): the
+  oracle checks O, LSE and dQ on query-row blocks at both ends of the sequence for
+  the first and the last head (each row against all keys); dK and dV, which need
+  every query per key, are checked through the identities sum_j dV_j = sum_i dO_i
+  and sum_j dK_j = 0 and through buffers filled with NaN before the call (every row
+  must be written);
+* the Ulysses re-layouts of four uneven shards of such a sequence: seq->head must
+  equal plain slicing of the concatenated sequence and head->seq must restore the
+  shards, bit for bit.
 """
 import math
 
@@ -37,10 +38,11 @@ def _release():
     torch.cuda.empty_cache()
 
 
-def test_many_problems_past_2_31_elements():
-    B, S, H, D = 640, 200, 136, 128
+@pytest.mark.parametrize("D", [128, 64])
+def test_many_problems_past_2_31_elements(D):
+    B, S, H = 640, 200, 136 * 128 // D
     assert B * S * H * D > 2 ** 31
-    inp = synth.draw_device(B, S, H, D, seed=31, device=DEV)
+    inp = synth.draw_device(B, S, H, D, seed=31 + D, device=DEV)
     q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
     g = torch.Generator().manual_seed(31)
     lens = torch.randint(1, S + 1, (B,), generator=g)
@@ -65,10 +67,11 @@ def test_many_problems_past_2_31_elements():
     _release()
 
 
-def test_long_sequence_past_2_31_elements():
-    B, S, H, D = 1, 131072, 136, 128
+@pytest.mark.parametrize("D", [128, 64])
+def test_long_sequence_past_2_31_elements(D):
+    B, S, H = 1, 131072, 136 * 128 // D
     assert B * S * H * D > 2 ** 31
-    inp = synth.draw_device(B, S, H, D, seed=37, device=DEV)
+    inp = synth.draw_device(B, S, H, D, seed=37 + D, device=DEV)
     q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
     scale = 1.0 / math.sqrt(D)
     o, lse = uaa.attn_fwd(q, k, v, None, scale)
