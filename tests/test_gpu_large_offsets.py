@@ -15,7 +15,11 @@ by the seeded generator of the input module:
   must be written);
 * the Ulysses re-layouts of four uneven shards of such a sequence: seq->head must
   equal plain slicing of the concatenated sequence and head->seq must restore the
-  shards, bit for bit.
+  shards, bit for bit;
+* the Ulysses step with the exchanges fused into the attention kernels on those
+  shards (one tensor map per shard): O, LSE and dQ rows at the ends of the first
+  and the last shard, first and last head, against the oracle on the whole
+  sequence, and every row of the output shards written.
 """
 import math
 
@@ -135,4 +139,37 @@ def test_relayouts_past_2_31_elements():
         assert torch.equal(back[p, :, :L].view(torch.int16), x[p, :, :L].view(torch.int16)), f"shard {p}"
         assert bool((back[p, :, L:].view(torch.int16) == 0).all()), f"padding rows of shard {p}"
     del x, y, back
+    _release()
+
+
+def test_fused_ulysses_past_2_31_elements():
+    lens, B, H, D = [32770, 32768, 32767, 32767], 1, 136, 128
+    P, cap, N = len(lens), max(lens), sum(lens)
+    assert P * B * cap * H * D > 2 ** 31
+    inp = synth.draw_device(P * B, cap, H, D, seed=43, device=DEV)  # (P*B, cap, H, D) = the shards
+    sh = {n: inp[n].view(P, B, cap, H, D) for n in ("q", "k", "v", "do")}
+    scale = 1.0 / math.sqrt(D)
+    o_sh, lse = uaa.ulysses_attn_fwd(sh["q"], sh["k"], sh["v"], lens, None, scale)
+    dq, dk, dv = (torch.full_like(sh["q"], float("nan")) for _ in range(3))
+    uaa.ulysses_attn_bwd(sh["q"], sh["k"], sh["v"], o_sh, sh["do"], lse, lens, None, scale, dq=dq, dk=dk, dv=dv)
+    uaa.check_device_status()
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    for t, name in ((o_sh, "O"), (dq, "dQ"), (dk, "dK"), (dv, "dV")):
+        for p, L in enumerate(lens):
+            assert bool(torch.isfinite(t[p, :, :L]).all()), f"{name}: rows of shard {p} left unwritten"
+    for h in (0, H - 1):
+        # the whole sequence of head h: the shards' valid rows in order
+        full = {n: torch.cat([sh[n][p, :, :L, h:h + 1] for p, L in enumerate(lens)], dim=1) for n in ("q", "k", "v", "do")}
+        kk, vv = f64(full["k"]), f64(full["v"])
+        for p, r0 in ((0, 0), (P - 1, lens[-1] - 128)):
+            n0 = int(offs[p]) + r0
+            qq, dd = f64(full["q"][:, n0:n0 + 128]), f64(full["do"][:, n0:n0 + 128])
+            ro, rl = oracle.attn_fwd(qq, kk, vv, None, scale)
+            rdq, _, _ = oracle.attn_bwd(qq, kk, vv, dd, None, scale)
+            label = f"h={h} shard {p} rows {r0}..{r0 + 127}"
+            compare(f"{label} O", f64(o_sh[p, :, r0:r0 + 128, h:h + 1]), ro, "o")
+            compare(f"{label} LSE", f64(lse[:, h:h + 1, n0:n0 + 128]), rl, "lse")
+            compare(f"{label} dQ", f64(dq[p, :, r0:r0 + 128, h:h + 1]), rdq, "dq")
+        del full
+    del inp, sh, o_sh, lse, dq, dk, dv
     _release()
