@@ -333,6 +333,17 @@ void uaa_set_wait_timeout_ms(unsigned int ms);
  * with a bad address: the load is simply not issued.  n < 0 turns it off. */
 void uaa_debug_drop_load(int n);
 
+/* Diagnostic (the pages have no counterpart): evaluates on the device, for
+ * tests, the exponential the forward kernel takes on the FMA pipe for one
+ * column pair of P in eight: 2^x by rounding x (clamped at -127) to n + f,
+ * |f| <= 1/2, a cubic in f fitted in relative error (the coefficients come from
+ * ulysses_dit_attention_gb300/exp2_fit.py; relative error below 8e-5) and 2^n
+ * written into the exponent field (exactly 0 for x <= -127 and -inf).
+ *   x, y : device float32 arrays of n elements, 8-byte aligned; n even
+ *   y[i] = that approximation of 2^x[i].
+ * Returns UAA_OK, UAA_ERR_INVALID_ARG or UAA_ERR_CUDA. */
+int uaa_debug_exp2_fma2(const float* x, float* y, long long n, uaa_stream_t stream);
+
 /* Thread-local, NUL-terminated message for the last non-OK status returned to
  * the calling thread ("" if none).  Owned by the library. */
 const char* uaa_last_error(void);

@@ -27,7 +27,7 @@ __all__ = [
     "UAAError", "lib", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_fused_workspace_bytes", "seq_to_head", "head_to_seq",
     "assemble_key_mask", "check_device_status", "watchdog_selftest", "set_wait_timeout_ms", "debug_drop_load",
     "set_bwd_profile_events", "Attention", "attn_fwd_groups", "attn_bwd_groups",
-    "attention", "UlyssesAttention", "ulysses_attention", "STATUS", "debug_build",
+    "attention", "UlyssesAttention", "ulysses_attention", "STATUS", "debug_build", "debug_exp2_fma2",
 ]
 
 STATUS = {0: "UAA_OK", -1: "UAA_ERR_INVALID_ARG", -2: "UAA_ERR_UNSUPPORTED", -3: "UAA_ERR_PER_HEAD_MASK",
@@ -76,6 +76,7 @@ _SIGS = {
     "uaa_last_error": (ctypes.c_char_p, []),
     "uaa_version": (ctypes.c_char_p, []),
     "uaa_debug_build": (_I, []),
+    "uaa_debug_exp2_fma2": (_I, [_P, _P, ctypes.c_longlong, _P]),
 }
 
 
@@ -387,6 +388,17 @@ def assemble_key_mask(gathered, shard_lens, out=None):
         out = torch.empty((B, sum(lens)), dtype=torch.uint8, device=gathered.device)
     _check(lib().uaa_assemble_key_mask(_ptr(gathered), _ptr(out), P, arr, cap, B, _P(_stream(gathered.device))))
     return out
+
+
+def debug_exp2_fma2(x):
+    """``uaa_debug_exp2_fma2``: the forward's FMA-pipe 2^x on a contiguous float32 CUDA tensor
+    with an even number of elements (a diagnostic for tests)."""
+    _need_cuda(x)
+    if x.dtype != torch.float32 or not x.is_contiguous() or x.numel() % 2:
+        raise ValueError("x must be a contiguous float32 tensor with an even number of elements")
+    y = torch.empty_like(x)
+    _check(lib().uaa_debug_exp2_fma2(_ptr(x), _ptr(y), x.numel(), _P(_stream(x.device))))
+    return y
 
 
 def debug_build() -> bool:

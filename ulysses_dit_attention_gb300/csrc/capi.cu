@@ -4,6 +4,7 @@
 // tensors, and the watchdog self-test kernel.
 #include <atomic>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 
@@ -147,6 +148,13 @@ int encode_seq_maps(SegMaps* maps, const void* ptr, const SeqDesc& d, int B, int
   return UAA_OK;
 }
 
+// exp2_fma2 (the forward's FMA-pipe exponential) over x[0 .. 2*npairs), pair by pair.
+__global__ void exp2_fma2_kernel(const float2* __restrict__ x, float2* __restrict__ y, long long npairs) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < npairs;
+       i += (long long)gridDim.x * blockDim.x)
+    y[i] = exp2_fma2(x[i]);
+}
+
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // runs out and records a timeout.  No copy or tensor-core work is issued.
 __global__ void watchdog_selftest_kernel(DevCtx ctx) {
@@ -221,6 +229,21 @@ int uaa_watchdog_selftest(unsigned int timeout_us, uaa_stream_t stream) {
   ctx.timeout_ns = (unsigned long long)timeout_us * 1000ull;
   watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ctx);
   return check_launch("uaa_watchdog_selftest");
+}
+
+int uaa_debug_exp2_fma2(const float* x, float* y, long long n, uaa_stream_t stream) {
+  if (n < 0 || (n & 1)) return set_error(UAA_ERR_INVALID_ARG, "uaa_debug_exp2_fma2: n must be even and >= 0");
+  if (n == 0) return UAA_OK;
+  if (!x || !y || (reinterpret_cast<uintptr_t>(x) & 7u) || (reinterpret_cast<uintptr_t>(y) & 7u))
+    return set_error(UAA_ERR_INVALID_ARG, "uaa_debug_exp2_fma2: x and y must be 8-byte aligned device arrays");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return set_error(UAA_ERR_CUDA, "uaa_debug_exp2_fma2: %s", cudaGetErrorString(e));
+  const long long pairs = n / 2, blocks = (pairs + 255) / 256, cap = (long long)sms * 8;
+  exp2_fma2_kernel<<<(int)(blocks < cap ? blocks : cap), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const float2*>(x), reinterpret_cast<float2*>(y), pairs);
+  return check_launch("uaa_debug_exp2_fma2");
 }
 
 }  // extern "C"
